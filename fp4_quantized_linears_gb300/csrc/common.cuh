@@ -1,0 +1,143 @@
+// common.cuh -- device helpers shared by the fp4lin kernels (sm_103a).
+//
+// Number formats of "Format-Aware Fusion for Fast FP4 Pretraining", Sec. 2.2:
+// E2M1 values, E8M0 and E4M3 block scales; Philox4x32-10 (Salmon et al.,
+// SC'11) for the stochastic rounding of Sec. 2.5.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp4lin.h"
+
+#define FP4_DEV __device__ __forceinline__
+
+namespace fp4 {
+
+// ---------------------------------------------------------------- status ---
+// Each translation unit keeps its own sticky status word; the API reads all.
+// The first error code wins.
+FP4_DEV void set_status(unsigned int* word, int code) { atomicCAS(word, 0u, (unsigned int)code); }
+
+// ----------------------------------------------------------------- bf16 ----
+FP4_DEV float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+FP4_DEV float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+FP4_DEV float bf16_to_f32(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+
+// Round-to-nearest-even binary32 -> bf16 bits (finite inputs).
+FP4_DEV uint16_t f32_to_bf16_rn(float f) {
+    uint32_t u = __float_as_uint(f);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+// --------------------------------------------------------------- E2M1 RN ---
+// Two binary32 values -> one byte of two E2M1 codes, `lo` in the low nibble,
+// round to nearest even with saturation at 6 (the hardware conversion).  The
+// sign of every input is copied into its code, so a negative value that
+// rounds to zero keeps its sign bit.
+FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    uint32_t s = ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
+    return r | s;
+}
+
+// --------------------------------------------------------------- E2M1 SR ---
+// Adjacent-bin stochastic rounding (Sec. 2.5, Eq. 9): with q- <= |v| < q+
+// neighbouring grid values, round up iff u * 2^-16 < (|v| - q-) / (q+ - q-);
+// |v| >= 6 saturates.  All steps are exact in binary32.
+FP4_DEV uint32_t e2m1_sr(float v, uint32_t u16) {
+    float a = fabsf(v);
+    uint32_t sign = (__float_as_uint(v) >> 31) << 3;
+    if (a >= 6.0f) return sign | 7u;
+    uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f);
+    // grid value of index lo and the reciprocal of the spacing to lo + 1
+    float qm = lo < 4 ? 0.5f * (float)lo : (lo == 4 ? 2.0f : (lo == 5 ? 3.0f : 4.0f));
+    float inv_sp = lo < 4 ? 2.0f : (lo < 6 ? 1.0f : 0.5f);
+    float p = __fmul_rn(__fsub_rn(a, qm), inv_sp);
+    uint32_t up = __fmul_rn((float)u16, 1.0f) < __fmul_rn(p, 65536.0f) ? 1u : 0u;
+    return sign | (lo + up);
+}
+
+// --------------------------------------------------------------- E4M3 ------
+// binary32 -> OCP E4M3 byte, round to nearest even, saturating at 448.
+FP4_DEV uint32_t e4m3_rn_satfinite(float s) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(s));
+    return (uint32_t)(r & 0xFFu);
+}
+
+// E4M3 byte (sign 0) -> binary32, exact.
+FP4_DEV float e4m3_value(uint32_t c) {
+    uint32_t E = (c >> 3) & 15u, m = c & 7u;
+    if (E == 0) return (float)m * 0.001953125f;  // m * 2^-9
+    return __uint_as_float(((E + 120u) << 23) | (m << 20));
+}
+
+// ------------------------------------------------------------ E8M0 (MX) ----
+// Upward E8M0 exponent of a block from the bit pattern of its amax (sign
+// cleared): the smallest e with 6 * 2^e >= amax, clamped to [-127, 127].
+// amax = f * 2^E with f in [1, 2): e = E - 2 if f <= 1.5 else E - 1.
+FP4_DEV int e8m0_exponent_up(uint32_t amax_bits) {
+    int field = (int)(amax_bits >> 23);
+    if (field == 0) return -127;  // zero or subnormal amax
+    int E = field - 127;
+    int e = (amax_bits & 0x7FFFFFu) <= 0x400000u ? E - 2 : E - 1;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as binary32 for e in [-126, 127] ... callers keep e <= 126.
+FP4_DEV float exp2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+
+// --------------------------------------------------------------- NVFP4 -----
+// Outer encode factor S_enc = fl32(2688 / amax) (Sec. 2.2.2); 1 for amax 0;
+// an overflow clamps to the largest finite binary32.
+FP4_DEV float nv_senc(float amax) {
+    if (amax == 0.0f) return 1.0f;
+    float s = __fdiv_rn(2688.0f, amax);
+    return isinf(s) ? 3.402823466e38f : s;
+}
+
+// Block scale byte and binary32 multiplier of one 16-value block:
+// s_raw = fl32(fl32(a_b / 6) * S_enc), delta = E4M3(s_raw),
+// m_b = delta == 0 ? 0 : fl32(S_enc / delta).
+FP4_DEV uint32_t nv_block_scale(float block_amax, float senc, float& mult) {
+    float s_raw = __fmul_rn(__fdiv_rn(block_amax, 6.0f), senc);
+    uint32_t d = e4m3_rn_satfinite(s_raw);
+    mult = d == 0 ? 0.0f : __fdiv_rn(senc, e4m3_value(d));
+    return d;
+}
+
+// -------------------------------------------------------------- Philox ----
+// Philox4x32-10: ten rounds of the 4x32 S-box with key increments.
+FP4_DEV uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// The eight 16-bit uniforms of elements 8g .. 8g+7 under (seed, offset).
+FP4_DEV uint4 sr_bits8(uint64_t g, uint64_t seed, uint64_t offset) {
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
+                         make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+}
+
+// ----------------------------------------------------------- scale layout --
+// Byte offset of block j of stored row r in the 128x4 atom layout, for a
+// view whose stored rows hold `nblk` blocks.
+__host__ __device__ inline int64_t scale_offset(int64_t r, int64_t j, int64_t nblk) {
+    return ((r >> 7) * (nblk >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (j & 3);
+}
+
+}  // namespace fp4

@@ -1,0 +1,437 @@
+// quantize.cu -- FP4 quantizer producers for sm_103a.
+//
+// One kernel emits, from a single read of each 128 x 128 BF16 tile, every view
+// the next contractions need ("Format-Aware Fusion for Fast FP4 Pretraining",
+// Sec. 3.1 boundary contract): the row-facing view Q_r (blocks along the row,
+// optionally stochastically rounded, Sec. 2.5 Eq. 9) and the column-facing view
+// Q_c (blocks along the column, optionally through the fixed-sign H32 of
+// Sec. 2.5 Eq. 10), with
+//   MXFP4         upward E8M0 scale per 32 values (Sec. 2.2.1),
+//   2D32 weights  one adaptive E8M0 per 32x32 tile, finer when a/s < 0.87,
+//   NVFP4         E4M3 scale per 16 values under the S_enc outer factor of
+//                 the tensor (global) or of the 128-strip (CTA-local),
+//                 (Sec. 2.2.2),
+//   2D16 weights  one E4M3 per 16x16 tile under the tensor factor (Sec. 2.4).
+// NVFP4 first runs a tile-amax pre-pass (the tensor-wide / strip-wide maximum
+// that the outer factors need), so its algorithmic traffic is two reads.
+//
+// Memory behaviour: coalesced 16-byte loads of the tile into shared memory,
+// per-thread 32-value segments for both orientations read from shared memory,
+// codes and scale atoms staged in shared memory and written with coalesced
+// 16-byte stores (each tile's scale bytes form whole 512-byte atoms).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp4 {
+
+__device__ unsigned int g_status_quant;
+
+namespace {
+
+constexpr int TILE = 128;
+constexpr int PAD = 8;               // bf16 elements of padding per smem row
+constexpr int LDS = TILE + PAD;      // smem row stride (elements)
+constexpr int THREADS = 256;
+
+struct SmemQ {
+    uint16_t tile[TILE * LDS];       // 34,816 B
+    uint8_t row_codes[TILE * 64];    // 8 KB staged row-view codes
+    uint8_t col_codes[TILE * 64];    // 8 KB staged column-view codes
+    uint8_t row_sc[1024];            // staged scale atoms (1 MX / 2 NV)
+    uint8_t col_sc[1024];
+    int tile_e[16];                  // 2D32: per 32x32 tile exponent
+    float tile_m[64];                // 2D16: per 16x16 tile multiplier
+    uint32_t tile_d[64];             // 2D16: per 16x16 tile E4M3 byte
+    uint32_t red[THREADS / 32];
+};
+
+// Byte offset of local block j (0..nb-1) of local row r in staged atoms.
+FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
+
+FP4_DEV uint32_t amax_bits32(const float* v) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    return m;
+}
+FP4_DEV uint32_t amax_bits16(const float* v) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    return m;
+}
+
+// Pack 32 E2M1 codes (RN) of v * mult into 16 bytes.
+FP4_DEV uint4 pack_rn32(const float* v, float mult) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            int i = q * 8 + b * 2;
+            word |= e2m1x2_rn(__fmul_rn(v[i], mult), __fmul_rn(v[i + 1], mult)) << (8 * b);
+        }
+        w[q] = word;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Two 16-blocks with their own multipliers.
+FP4_DEV uint4 pack_rn16x2(const float* v, float m0, float m1) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float mult = q < 2 ? m0 : m1;
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            int i = q * 8 + b * 2;
+            word |= e2m1x2_rn(__fmul_rn(v[i], mult), __fmul_rn(v[i + 1], mult)) << (8 * b);
+        }
+        w[q] = word;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Stochastic rounding of 32 values (logical indices 8*g0 .. 8*g0+31).
+FP4_DEV uint4 pack_sr32(const float* v, float m0, float m1, uint64_t g0, uint64_t seed, uint64_t offset) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 rb = sr_bits8(g0 + q, seed, offset);
+        uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
+        float mult = q < 2 ? m0 : m1;
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            int i = q * 8 + b * 2;
+            uint32_t c0 = e2m1_sr(__fmul_rn(v[i], mult), rw[b] & 0xFFFFu);
+            uint32_t c1 = e2m1_sr(__fmul_rn(v[i + 1], mult), rw[b] >> 16);
+            word |= (c0 | (c1 << 4)) << (8 * b);
+        }
+        w[q] = word;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Fixed-sign H32 on 32 registers: signs, butterflies of stride 1..16, 1/sqrt(32).
+FP4_DEV void hadamard32(float* v, uint32_t neg_mask) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((neg_mask >> (i & 15)) & 1u) << 31));
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if ((j & h) == 0) {
+                float a = v[j], b = v[j + h];
+                v[j] = __fadd_rn(a, b);
+                v[j + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+    const float s = __uint_as_float(0x3E3504F3u);  // fl32(1 / sqrt(32))
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], s);
+}
+
+FP4_DEV void check_finite(uint32_t amax_bits) {
+    if (amax_bits >= 0x7F800000u) set_status(&g_status_quant, FP4_ERR_NONFINITE);
+}
+
+// Quantize one 32-value segment (MX: one block; NV: two blocks) and stage its
+// codes (16 B at code_dst) and scale bytes.
+template <bool NV>
+FP4_DEV void encode_segment(float* v, bool sr, uint64_t g0, const QuantParams& p, float senc, int fixed_e,
+                            uint32_t fixed_d0, uint32_t fixed_d1, float fixed_m0, float fixed_m1, bool fixed,
+                            uint8_t* code_dst, uint8_t* sc_base, int lr, int lj) {
+    uint4 packed;
+    if (!NV) {
+        int e;
+        if (fixed) {
+            e = fixed_e;
+        } else {
+            uint32_t am = amax_bits32(v);
+            check_finite(am);
+            e = e8m0_exponent_up(am);
+        }
+        float mult = exp2_neg(e);
+        packed = sr ? pack_sr32(v, mult, mult, g0, p.seed, p.offset) : pack_rn32(v, mult);
+        sc_base[atom_off(lr, lj)] = (uint8_t)(e + 127);
+    } else {
+        uint32_t d0, d1;
+        float m0, m1;
+        if (fixed) {
+            d0 = fixed_d0; d1 = fixed_d1; m0 = fixed_m0; m1 = fixed_m1;
+        } else {
+            uint32_t a0 = amax_bits16(v), a1 = amax_bits16(v + 16);
+            check_finite(max(a0, a1));
+            d0 = nv_block_scale(__uint_as_float(a0), senc, m0);
+            d1 = nv_block_scale(__uint_as_float(a1), senc, m1);
+        }
+        packed = sr ? pack_sr32(v, m0, m1, g0, p.seed, p.offset) : pack_rn16x2(v, m0, m1);
+        sc_base[atom_off(lr, 2 * lj)] = (uint8_t)d0;
+        sc_base[atom_off(lr, 2 * lj + 1)] = (uint8_t)d1;
+    }
+    *reinterpret_cast<uint4*>(code_dst) = packed;
+}
+
+template <bool NV>
+__global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
+    const int t = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.y * TILE, c0 = (int64_t)blockIdx.x * TILE;
+    const bool w2d = (p.flags & FP4_FLAG_WEIGHT_2D) != 0;
+    const bool do_row = (p.views & FP4_VIEW_ROW) != 0, do_col = (p.views & FP4_VIEW_COL) != 0;
+
+    // 1. tile -> shared memory (16-byte coalesced loads)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int q = t + i * THREADS;
+        int rr = q >> 4, cc = (q & 15) * 8;
+        uint4 d = *reinterpret_cast<const uint4*>(p.x + (r0 + rr) * p.ld + c0 + cc);
+        *reinterpret_cast<uint4*>(&s.tile[rr * LDS + cc]) = d;
+    }
+
+    // outer factors of this tile's row strip / column strip
+    float senc_row = 1.0f, senc_col = 1.0f;
+    if (NV) {
+        const uint32_t* ws = p.amax_ws;
+        if (p.route == FP4_ROUTE_NVFP4_GLOBAL || w2d) {
+            senc_row = senc_col = nv_senc(__uint_as_float(ws[0]));
+        } else {
+            senc_row = nv_senc(__uint_as_float(ws[1 + blockIdx.y]));
+            senc_col = nv_senc(__uint_as_float(ws[1 + (p.R >> 7) + blockIdx.x]));
+        }
+        if (t == 0) {
+            if (p.route == FP4_ROUTE_NVFP4_LOCAL && !w2d) {
+                if (do_row && blockIdx.x == 0) p.row_outer[blockIdx.y] = senc_row;
+                if (do_col && blockIdx.y == 0) p.col_outer[blockIdx.x] = senc_col;
+            } else if (blockIdx.x == 0 && blockIdx.y == 0) {
+                if (do_row) p.row_outer[0] = senc_row;
+                if (do_col) p.col_outer[0] = senc_col;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 2. shared 2D weight scales
+    if (w2d) {
+        const int warp = t >> 5, lane = t & 31;
+        if (!NV) {
+            // 16 tiles of 32x32: warp w handles tiles 2w, 2w+1; lane = row
+            for (int k = 0; k < 2; ++k) {
+                int tile = warp * 2 + k, tr = tile >> 2, tc = tile & 3;
+                uint32_t m = 0;
+                const uint16_t* row = &s.tile[(tr * 32 + lane) * LDS + tc * 32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) m = max(m, ((uint32_t)row[j] << 16) & 0x7FFFFFFFu);
+#pragma unroll
+                for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                if (lane == 0) {
+                    check_finite(m);
+                    int e = e8m0_exponent_up(m);
+                    // adaptive rule: finer exponent when a_T * 2^-e < fl32(5.22)
+                    if (__fmul_rn(__uint_as_float(m), exp2_neg(e)) < 5.22f && e > -127) e -= 1;
+                    s.tile_e[tile] = e;
+                }
+            }
+        } else {
+            // 64 tiles of 16x16: warp w handles tiles 8w .. 8w+7, two at a time
+            for (int k = 0; k < 4; ++k) {
+                int tile = warp * 8 + k * 2 + (lane >> 4), tr = tile >> 3, tc = tile & 7;
+                const uint16_t* row = &s.tile[(tr * 16 + (lane & 15)) * LDS + tc * 16];
+                uint32_t m = 0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) m = max(m, ((uint32_t)row[j] << 16) & 0x7FFFFFFFu);
+#pragma unroll
+                for (int o = 8; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                if ((lane & 15) == 0) {
+                    check_finite(m);
+                    float mm;
+                    s.tile_d[tile] = nv_block_scale(__uint_as_float(m), senc_row, mm);
+                    s.tile_m[tile] = mm;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // 3. row-facing view: segment (r, j) = 32 values of local row r starting at 32 j
+    if (do_row) {
+        const bool sr = (p.flags & FP4_FLAG_SR_ROW) != 0;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
+            float v[32];
+            const uint16_t* src = &s.tile[r * LDS + j * 32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
+                uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    v[q * 8 + 2 * b] = bf16_lo(w[b]);
+                    v[q * 8 + 2 * b + 1] = bf16_hi(w[b]);
+                }
+            }
+            uint64_t g0 = (uint64_t)(((r0 + r) * p.C + c0 + 32 * j) >> 3);
+            int fe = 0;
+            uint32_t d0 = 0, d1 = 0;
+            float m0 = 0.f, m1 = 0.f;
+            if (w2d) {
+                if (!NV) {
+                    fe = s.tile_e[(r >> 5) * 4 + j];
+                } else {
+                    int tl = (r >> 4) * 8 + 2 * j;
+                    d0 = s.tile_d[tl]; d1 = s.tile_d[tl + 1];
+                    m0 = s.tile_m[tl]; m1 = s.tile_m[tl + 1];
+                }
+            }
+            encode_segment<NV>(v, sr, g0, p, senc_row, fe, d0, d1, m0, m1, w2d, &s.row_codes[r * 64 + j * 16],
+                               s.row_sc, r, j);
+        }
+    }
+
+    // 4. column-facing view: segment (c, j) = 32 values of local column c
+    //    starting at local row 32 j (stored row c, blocks along the rows)
+    if (do_col) {
+        const bool had = (p.flags & FP4_FLAG_HADAMARD_COL) != 0;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            int idx = t + k * THREADS, j = idx >> 7, c = idx & 127;
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = bf16_to_f32(s.tile[(j * 32 + i) * LDS + c]);
+            if (had) hadamard32(v, p.sign_mask);
+            int fe = 0;
+            uint32_t d0 = 0, d1 = 0;
+            float m0 = 0.f, m1 = 0.f;
+            if (w2d) {
+                if (!NV) {
+                    fe = s.tile_e[j * 4 + (c >> 5)];
+                } else {
+                    int tl = (2 * j) * 8 + (c >> 4);
+                    d0 = s.tile_d[tl]; d1 = s.tile_d[tl + 8];
+                    m0 = s.tile_m[tl]; m1 = s.tile_m[tl + 8];
+                }
+            }
+            encode_segment<NV>(v, false, 0, p, senc_col, fe, d0, d1, m0, m1, w2d, &s.col_codes[c * 64 + j * 16],
+                               s.col_sc, c, j);
+        }
+    }
+    __syncthreads();
+
+    // 5. coalesced write-out of staged codes and scale atoms
+    if (do_row) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            int q = t + k * THREADS, rr = q >> 2, part = q & 3;
+            *reinterpret_cast<uint4*>(p.row_codes + (r0 + rr) * (p.C >> 1) + (c0 >> 1) + part * 16) =
+                *reinterpret_cast<const uint4*>(&s.row_codes[rr * 64 + part * 16]);
+        }
+        const int nat = NV ? 2 : 1;
+        if (t < nat * 32) {
+            int64_t atoms_per_rowblock = NV ? (p.C >> 6) : (p.C >> 7);
+            int64_t a0 = (r0 >> 7) * atoms_per_rowblock + (NV ? (c0 >> 6) : (c0 >> 7));
+            *reinterpret_cast<uint4*>(p.row_scales + a0 * 512 + t * 16) =
+                *reinterpret_cast<const uint4*>(&s.row_sc[t * 16]);
+        }
+    }
+    if (do_col) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            int q = t + k * THREADS, cc = q >> 2, part = q & 3;
+            *reinterpret_cast<uint4*>(p.col_codes + (c0 + cc) * (p.R >> 1) + (r0 >> 1) + part * 16) =
+                *reinterpret_cast<const uint4*>(&s.col_codes[cc * 64 + part * 16]);
+        }
+        const int nat = NV ? 2 : 1;
+        if (t < nat * 32) {
+            int64_t atoms_per_rowblock = NV ? (p.R >> 6) : (p.R >> 7);
+            int64_t a0 = (c0 >> 7) * atoms_per_rowblock + (NV ? (r0 >> 6) : (r0 >> 7));
+            *reinterpret_cast<uint4*>(p.col_scales + a0 * 512 + t * 16) =
+                *reinterpret_cast<const uint4*>(&s.col_sc[t * 16]);
+        }
+    }
+}
+
+// Tile-amax pre-pass for NVFP4: max |x| of each 128x128 tile folded into the
+// tensor slot ws[0], the tile's row-strip slot and its column-strip slot.
+__global__ void __launch_bounds__(THREADS) nv_amax_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t ld,
+                                                         uint32_t* ws, int64_t n_row_strips) {
+    __shared__ uint32_t red[THREADS / 32];
+    const int t = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.y * TILE, c0 = (int64_t)blockIdx.x * TILE;
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int q = t + i * THREADS;
+        int rr = q >> 4, cc = (q & 15) * 8;
+        uint4 d = *reinterpret_cast<const uint4*>(x + (r0 + rr) * ld + c0 + cc);
+        uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            m = max(m, (w[b] << 16) & 0x7FFFFFFFu);
+            m = max(m, w[b] & 0x7FFF0000u);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((t & 31) == 0) red[t >> 5] = m;
+    __syncthreads();
+    if (t == 0) {
+        for (int i = 1; i < THREADS / 32; ++i) m = max(m, red[i]);
+        check_finite(m);
+        atomicMax(&ws[0], m);
+        atomicMax(&ws[1 + blockIdx.y], m);
+        atomicMax(&ws[1 + n_row_strips + blockIdx.x], m);
+    }
+}
+
+}  // namespace
+
+int launch_quantize(const QuantParams& p, cudaStream_t stream) {
+    dim3 grid((unsigned)(p.C / TILE), (unsigned)(p.R / TILE));
+    const size_t smem = sizeof(SmemQ);
+    const bool nv = p.route != FP4_ROUTE_MXFP4;
+    if (nv) {
+        size_t ws_bytes = (size_t)(1 + p.R / TILE + p.C / TILE) * 4;
+        if (cudaMemsetAsync(p.amax_ws, 0, ws_bytes, stream) != cudaSuccess) return FP4_ERR_CUDA;
+        nv_amax_kernel<<<grid, THREADS, 0, stream>>>(p.x, p.R, p.ld, p.amax_ws, p.R / TILE);
+        if (cudaGetLastError() != cudaSuccess) return FP4_ERR_CUDA;
+        static bool attr_nv = false;
+        if (!attr_nv) {
+            cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            attr_nv = true;
+        }
+        quantize_tile_kernel<true><<<grid, THREADS, smem, stream>>>(p);
+    } else {
+        static bool attr_mx = false;
+        if (!attr_mx) {
+            cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            attr_mx = true;
+        }
+        quantize_tile_kernel<false><<<grid, THREADS, smem, stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
+int quant_status(cudaStream_t stream, int* code, bool reset) {
+    unsigned int v = 0;
+    if (reset) {
+        return cudaMemcpyToSymbolAsync(g_status_quant, &v, sizeof v, 0, cudaMemcpyHostToDevice, stream) == cudaSuccess
+                   ? FP4_OK
+                   : FP4_ERR_CUDA;
+    }
+    if (cudaMemcpyFromSymbolAsync(&v, g_status_quant, sizeof v, 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return FP4_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FP4_ERR_CUDA;
+    *code = (int)v;
+    return FP4_OK;
+}
+
+}  // namespace fp4

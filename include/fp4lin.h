@@ -1,0 +1,192 @@
+/*
+ * fp4lin.h -- C ABI of the format-aware FP4 linear-layer boundary
+ * ("Format-Aware Fusion for Fast FP4 Pretraining"), hand-written CUDA for
+ * sm_103a (GB300).
+ *
+ * Two halves, as in the paper's boundary contract (Sec. 3.1):
+ *   producers  fp4_quantize, fp4_swiglu_fwd/bwd, fp4_residual_rmsnorm_fwd/bwd
+ *              turn BF16 tensors into E2M1 codes plus scales in the physical
+ *              layout the next contraction consumes;
+ *   consumers  fp4_linear_fprop/dgrad/wgrad, block-scaled tcgen05 GEMMs.
+ *
+ * General conventions
+ *  - Every pointer named "device" is caller-owned CUDA device memory.  The
+ *    library never allocates, frees or synchronises; each call enqueues its
+ *    kernels on `stream` and returns.  Host pointers are read during the call
+ *    only.
+ *  - Every call returns an fp4 status code (FP4_OK == 0).  Argument errors are
+ *    detected on the host before anything is enqueued.  Device-side conditions
+ *    (non-finite input, a bounded wait that ran out) set a sticky device status
+ *    word that fp4_status() reads.
+ *  - BF16 tensors are row-major with a leading dimension `ld` in elements
+ *    (ld >= cols, ld % 8 == 0, base 16-byte aligned).
+ *
+ * Quantized tensor layout (fp4_tensor)
+ *  A quantized view is stored K-major: `rows` stored rows of `cols` values,
+ *  where cols is the reduction axis K of the consuming contraction.
+ *   - The row-facing view Q_r(T) of a logical R x C tensor T has rows = R,
+ *     cols = C.  The column-facing view Q_c(T) has rows = C, cols = R (it holds
+ *     T transposed).  (Sec. 2.3, Eqs. 4-6.)
+ *   - codes: rows * cols / 2 bytes; stored row r occupies bytes
+ *     [r * cols/2, (r+1) * cols/2); value k of the row sits in byte k/2, in the
+ *     low nibble when k is even and the high nibble when k is odd.  A nibble is
+ *     an E2M1 code: bit 3 sign, bits 2..1 exponent, bit 0 fraction.
+ *   - scales: one byte per block of bs values along a stored row (bs = 32,
+ *     E8M0, for MXFP4; bs = 16, E4M3, for NVFP4).  The bytes are grouped in
+ *     512-byte atoms of 128 stored rows x 4 consecutive blocks:
+ *       atom  = (r / 128) * (cols / (4 * bs)) + (j / 4)     j = k / bs
+ *       byte  = atom * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (j % 4)
+ *     which is the layout the tcgen05 block-scaled MMA reads after a
+ *     32x128b.warpx4 copy into tensor memory.  scale bytes = rows * cols / bs.
+ *   - outer: NVFP4 encode factors S_enc (binary32).  outer_count = 1 for global
+ *     NVFP4 and for every 2D16 weight; rows / 128 (one per 128-row strip of the
+ *     stored view) for CTA-local activations and gradients; 0 and NULL for
+ *     MXFP4.  Decoded value = code * block scale / S_enc.
+ *  Shape rules: rows % 128 == 0 and cols % 128 == 0.
+ */
+#ifndef FP4LIN_H
+#define FP4LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP4LIN_VERSION 100 /* 1.0.0 */
+
+/* Exported symbols keep default visibility (the library builds with hidden
+ * visibility for everything else). */
+#if defined(__GNUC__)
+#define FP4_API __attribute__((visibility("default")))
+#else
+#define FP4_API
+#endif
+
+/* A cudaStream_t.  NULL selects the legacy default stream. */
+typedef struct CUstream_st* fp4_stream_t;
+
+/* Status codes. */
+enum fp4_status_code {
+    FP4_OK = 0,
+    FP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, bad leading dimension */
+    FP4_ERR_UNSUPPORTED_SHAPE = 2, /* a dimension breaks the shape rules */
+    FP4_ERR_ROUTE_MISMATCH = 3,    /* operands of different routes / a flag the route forbids */
+    FP4_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required */
+    FP4_ERR_CUDA = 5,              /* a CUDA runtime call failed */
+    FP4_ERR_TIMEOUT = 6,           /* (device) a bounded pipeline wait ran out */
+    FP4_ERR_NONFINITE = 7          /* (device) a quantizer saw Inf or NaN */
+};
+
+/* Routes: the three scale contracts of Sec. 2.2. */
+enum fp4_route {
+    FP4_ROUTE_MXFP4 = 0,        /* 32-value blocks, upward-rounded E8M0 scales (Sec. 2.2.1) */
+    FP4_ROUTE_NVFP4_GLOBAL = 1, /* 16-value E4M3 blocks under one tensor-amax factor (Sec. 2.2.2) */
+    FP4_ROUTE_NVFP4_LOCAL = 2   /* 16-value E4M3 blocks under per-128-strip factors (Sec. 2.2.2, Eq. 3) */
+};
+
+/* Views requested from a producer (bit mask). */
+enum fp4_view { FP4_VIEW_ROW = 1, FP4_VIEW_COL = 2 };
+
+/* Producer flags (bit mask). */
+enum fp4_flag {
+    FP4_FLAG_WEIGHT_2D = 1,     /* 2D32 (MX, adaptive finer scale when a/s < 0.87) or 2D16 (NV) weight
+                                   encoding shared by both views (Sec. 2.4, Eqs. 7-8) */
+    FP4_FLAG_SR_ROW = 2,        /* stochastic rounding of the row view (Sec. 2.5, Eq. 9) */
+    FP4_FLAG_HADAMARD_COL = 4   /* fixed-sign H32 on the column view before quantization
+                                   (Sec. 2.5, Eq. 10; MXFP4 only) */
+};
+
+/* GEMM output element types. */
+enum fp4_out_dtype { FP4_OUT_F32 = 0, FP4_OUT_BF16 = 1 };
+
+/* One quantized view.  All pointers are caller-owned device memory sized by
+ * fp4_tensor_bytes(); the producer fills every field. */
+typedef struct fp4_tensor {
+    void* codes;         /* device, rows * cols / 2 bytes */
+    void* scales;        /* device, rows * cols / bs bytes, atom layout above */
+    float* outer;        /* device, outer_count binary32 S_enc values, or NULL */
+    int64_t rows;        /* stored rows (M or N of the consumer) */
+    int64_t cols;        /* stored columns (K of the consumer) */
+    int32_t route;       /* enum fp4_route */
+    int32_t outer_count; /* 0, 1 or rows / 128 */
+} fp4_tensor;
+
+/* Library version (FP4LIN_VERSION). */
+FP4_API int fp4_version(void);
+
+/* Human-readable name of a status code (static string). */
+FP4_API const char* fp4_status_string(int code);
+
+/* Sizes of one quantized view with `rows` stored rows of `cols` values:
+ * codes and scale bytes, and the number of S_enc values (0 for MXFP4; 1 for
+ * global NVFP4 or with FP4_FLAG_WEIGHT_2D; rows / 128 for CTA-local).
+ * Host only; nothing is enqueued. */
+FP4_API int fp4_tensor_bytes(int route, int64_t rows, int64_t cols, unsigned flags, size_t* codes_bytes,
+                     size_t* scale_bytes, int32_t* outer_count);
+
+/* Workspace bytes fp4_quantize needs for this route and shape (0 for MXFP4;
+ * (1 + rows/128 + cols/128) * 4 for NVFP4, the amax slots of the outer-factor
+ * pre-pass).  Host only. */
+FP4_API int fp4_quantize_workspace_bytes(int route, int64_t rows, int64_t cols, unsigned views, unsigned flags,
+                                 size_t* bytes);
+
+/* Quantize a BF16 tensor x (device, rows x cols, leading dimension ld) into
+ * the requested views (Sec. 2.2-2.5, Sec. 3.1).
+ *  route          enum fp4_route
+ *  views          FP4_VIEW_ROW and/or FP4_VIEW_COL
+ *  flags          FP4_FLAG_WEIGHT_2D: one shared 2D encoding (views decode
+ *                 identically, Eq. 8; no SR, no H32);
+ *                 FP4_FLAG_SR_ROW: Philox4x32-10 stochastic rounding of the row
+ *                 view only; element i = r * cols + c of the logical tensor uses
+ *                 16 bits of Philox(key = sr_seed, counter = (i/8, sr_offset)),
+ *                 word (i%8)/2, low half for even i;
+ *                 FP4_FLAG_HADAMARD_COL: H32 = Sylvester H32 x diag(signs
+ *                 repeated over both halves) / sqrt(32) on every aligned
+ *                 32-value block of the column view (MXFP4 only).
+ *  hadamard_signs host array of 16 int8 values, each +1 or -1 (read only when
+ *                 FP4_FLAG_HADAMARD_COL is set).
+ *  row_out/col_out caller-filled codes/scales/outer pointers for each requested
+ *                 view (may be NULL for a view not requested); the call sets
+ *                 rows, cols, route and outer_count.
+ *  workspace      device scratch of fp4_quantize_workspace_bytes() bytes
+ *                 (NULL allowed when that is 0); its contents are overwritten.
+ * Errors: FP4_ERR_INVALID_ARG, FP4_ERR_UNSUPPORTED_SHAPE (rows or cols not a
+ * multiple of 128), FP4_ERR_ROUTE_MISMATCH (SR with WEIGHT_2D, H32 on NVFP4 or
+ * with WEIGHT_2D), FP4_ERR_WORKSPACE, FP4_ERR_CUDA (launch failure). */
+FP4_API int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int route, unsigned views,
+                 unsigned flags, uint64_t sr_seed, uint64_t sr_offset, const int8_t* hadamard_signs,
+                 fp4_tensor* row_out, fp4_tensor* col_out, void* workspace, size_t workspace_bytes,
+                 fp4_stream_t stream);
+
+/* The three contractions of Sec. 2.3 (Eqs. 4-6).  Each computes
+ *   C[m][n] = alpha(m, n) * sum_k A_hat[m][k] * B_hat[n][k] + beta * C[m][n]
+ * over K-major operands with FP32 tensor-core accumulation, where A_hat/B_hat
+ * are code * block scale and alpha = 1 (MXFP4) or 1 / (S_enc,A * S_enc,B)
+ * with the factor of each operand's row strip (NVFP4; the CTA-local epilogue
+ * of Sec. 2.2.2).  Output C is row-major [M][N] (ldc = N) in out_dtype; beta
+ * = 0 does not read C.  A.cols == B.cols, M % 128 == 0, N % 128 == 0,
+ * K % 256 == 0; both operands of one route.
+ *   fprop:  Y  [T x out] = Q_r(X)  [T x in]  . Q_r(W)  [out x in]^T
+ *   dgrad:  dX [T x in]  = Q_r(dY) [T x out] . Q_c(W)  [in x out]^T
+ *   wgrad:  dW [out x in]= Q_c(dY) [out x T] . Q_c(X)  [in x T]^T   (FP32 only) */
+FP4_API int fp4_linear_fprop(const fp4_tensor* x_row, const fp4_tensor* w_row, void* y, int out_dtype, float beta,
+                     fp4_stream_t stream);
+FP4_API int fp4_linear_dgrad(const fp4_tensor* dy_row, const fp4_tensor* w_col, void* dx, int out_dtype, float beta,
+                     fp4_stream_t stream);
+FP4_API int fp4_linear_wgrad(const fp4_tensor* dy_col, const fp4_tensor* x_col, float* dw, float beta,
+                     fp4_stream_t stream);
+
+/* Read the sticky device status word (first device-side error since the last
+ * reset, FP4_OK if none) into *code.  Synchronises `stream`. */
+FP4_API int fp4_status(fp4_stream_t stream, int* code);
+
+/* Clear the sticky device status word (enqueued on `stream`). */
+FP4_API int fp4_status_reset(fp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4LIN_H */
