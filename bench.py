@@ -1,0 +1,422 @@
+"""Benchmark of the FP4 linear boundary on one GB300.
+
+One step = one pass of the whole boundary over one batch of seeded synthetic
+input at the Llama-3-8B W1 shape ("MXFP4 Llama-3-8B W1-shaped linear"):
+    producers  X [8192 x 4096]  -> Q_r(X), Q_c(X) with fixed-sign H32
+               W [14336 x 4096] -> 2D32 Q_r(W), Q_c(W)
+               dY [8192 x 14336]-> Q_r(dY) with Philox SR, Q_c(dY) with H32
+    GEMMs      Fprop Y = X W^T, Dgrad dX = dY W, Wgrad dW = dY^T X (FP32 out)
+value = 3 * 2*M*N*K FP4 FLOPs / step time (TFLOP/s), with tokens/s and the
+producers' algorithmic GB/s alongside.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica of the step (weak
+scaling, no data-path collective); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Fprop+Dgrad+Wgrad FP4 TFLOPS and tokens/s at Llama-3-8B shapes; quant GB/s"
+WORKLOAD = "mxfp4_llama3_8b_w1_linear"
+T, D_IN, D_OUT = 8192, 4096, 14336
+FP4_NOMINAL_OVER_BF16 = 13.5 / 2.25  # dense FP4 / dense BF16 nominal ratio on GB300
+
+
+def flops_per_step() -> float:
+    return 3 * 2.0 * T * D_IN * D_OUT
+
+
+def producer_bytes() -> dict:
+    # algorithmic bytes: 2 B/elem read + per view 0.5 B codes + 1/32 B E8M0 scales
+    mx_both = 2 + 2 * (0.5 + 1 / 32)
+    return dict(x=T * D_IN * mx_both, w=D_OUT * D_IN * mx_both, dy=T * D_OUT * mx_both)
+
+
+def gemm_bytes_min() -> float:
+    return 0.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- distributed ----
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("FP4_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, local, world, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None and pg.get_backend() == "nccl":
+            pg.barrier(device_ids=[device])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, v: float) -> float:
+    if pg is None:
+        return v
+    import torch
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- our arm ----
+def run_ours(args):
+    import torch
+    import fp4_quantized_linears_gb300 as F
+    from synthetic import config_tensors
+
+    rank, local, world, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    F.load()
+    t0 = time.time()
+    host = config_tensors("c2_mx_w1", scale_T=T)
+    signs = [int(s) for s in host["signs"]]
+
+    def to_dev(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X, W, DY = to_dev(host["x"]), to_dev(host["w"]), to_dev(host["dy"])
+    gen_s = time.time() - t0
+    # persistent outputs (allocated once, outside the timed region)
+    xr, xc = F.alloc_view("mx", T, D_IN), F.alloc_view("mx", D_IN, T)
+    wr, wc = F.alloc_view("mx", D_OUT, D_IN), F.alloc_view("mx", D_IN, D_OUT)
+    dr, dc = F.alloc_view("mx", T, D_OUT), F.alloc_view("mx", D_OUT, T)
+    Y = torch.empty((T, D_OUT), dtype=torch.float32, device=dev)
+    DX = torch.empty((T, D_IN), dtype=torch.float32, device=dev)
+    DW = torch.empty((D_OUT, D_IN), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    names = ["quant_x", "quant_w", "quant_dy", "fprop", "dgrad", "wgrad"]
+
+    def step(ev=None, seed_offset=0, x=X, w=W, dy=DY):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        F.fp4_quantize(x, "mx", 3, F.FP4_FLAG_HADAMARD_COL, hadamard_signs=signs, row_out=xr, col_out=xc)
+        mark(1)
+        F.fp4_quantize(w, "mx", 3, F.FP4_FLAG_WEIGHT_2D, row_out=wr, col_out=wc)
+        mark(2)
+        F.fp4_quantize(dy, "mx", 3, F.FP4_FLAG_SR_ROW | F.FP4_FLAG_HADAMARD_COL, sr_seed=1, sr_offset=seed_offset,
+                       hadamard_signs=signs, row_out=dr, col_out=dc)
+        mark(3)
+        F.fp4_linear_fprop(xr, wr, Y)
+        mark(4)
+        F.fp4_linear_dgrad(dr, wc, DX)
+        mark(5)
+        F.fp4_linear_wgrad(dc, xc, DW)
+        mark(6)
+
+    for i in range(args.warmup):
+        step(seed_offset=i)
+    torch.cuda.synchronize()
+    if F.fp4_status() != F.FP4_OK:
+        raise RuntimeError("device status set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i], seed_offset=1000 + i)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, local)
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    total_ms = max_over_ranks(pg, total_ms)
+    per_kernel = {n: statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps))
+                  for k, n in enumerate(names)}
+    if F.fp4_status() != F.FP4_OK:
+        raise RuntimeError("device status set during the timed region")
+
+    # end to end through the public API with pinned host buffers
+    pin = (lambda t: t) if args.no_e2e else (lambda t: t.pin_memory())
+    hx = pin(torch.from_numpy(host["x"].view(np.int16)).view(torch.bfloat16))
+    hw = pin(torch.from_numpy(host["w"].view(np.int16)).view(torch.bfloat16))
+    hdy = pin(torch.from_numpy(host["dy"].view(np.int16)).view(torch.bfloat16))
+    hY = pin(torch.empty(Y.shape, dtype=torch.float32))
+    hDX = pin(torch.empty(DX.shape, dtype=torch.float32))
+    hDW = pin(torch.empty(DW.shape, dtype=torch.float32))
+    dX2, dW2, dDY2 = (None, None, None) if args.no_e2e else (torch.empty_like(X), torch.empty_like(W), torch.empty_like(DY))
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step(i):
+        dX2.copy_(hx, non_blocking=True)
+        dW2.copy_(hw, non_blocking=True)
+        dDY2.copy_(hdy, non_blocking=True)
+        step(seed_offset=5000 + i, x=dX2, w=dW2, dy=dDY2)
+        hY.copy_(Y, non_blocking=True)
+        hDX.copy_(DX, non_blocking=True)
+        hDW.copy_(DW, non_blocking=True)
+
+    e2e_ms = float("nan")
+    if not args.no_e2e:
+        e2e_step(0)
+        torch.cuda.synchronize()
+        barrier(pg, local)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i + 1)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1) / e2e_steps)
+    h2d = (hx.numel() + hw.numel() + hdy.numel()) * 2
+    d2h = (hY.numel() + hDX.numel() + hDW.numel()) * 4
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+
+    ms = total_ms / args.steps
+    tflops = flops_per_step() / (ms * 1e-3) / 1e12 * world
+    pb = producer_bytes()
+    quant_ms = per_kernel["quant_x"] + per_kernel["quant_w"] + per_kernel["quant_dy"]
+    quant_gbs = (pb["x"] + pb["w"] + pb["dy"]) / (quant_ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    fp4_peak = peaks["bf16"] * FP4_NOMINAL_OVER_BF16
+    gemm_flops = 2.0 * T * D_IN * D_OUT
+    # dominant kernel by time share
+    dom = max(per_kernel, key=per_kernel.get)
+    if dom in ("fprop", "dgrad", "wgrad"):
+        ach = gemm_flops / (per_kernel[dom] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp4_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp4_peak, 4), "traffic": None,
+                "peak_note": f"{peaks['src']} bf16 burst {peaks['bf16']} x nominal fp4/bf16 ratio 6"}
+    else:
+        b = pb[dom.split("_")[1]]
+        ach = b / (per_kernel[dom] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm"], 4), "traffic": None, "peak_note": f"{peaks['src']} hbm_gbs"}
+    kernels = {}
+    for n, v in per_kernel.items():
+        if n.startswith("quant"):
+            b = pb[n.split("_")[1]]
+            kernels[n] = {"ms": round(v, 4), "GB/s": round(b / (v * 1e-3) / 1e9, 1),
+                          "hbm_frac": round(b / (v * 1e-3) / 1e9 / peaks["hbm"], 4)}
+        else:
+            tf = gemm_flops / (v * 1e-3) / 1e12
+            kernels[n] = {"ms": round(v, 4), "TFLOP/s": round(tf, 1), "fp4_frac": round(tf / fp4_peak, 4)}
+
+    cpu = cpu_baseline_sample(seconds_target=args.cpu_seconds) if args.cpu_seconds > 0 else None
+    line = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1", "data": "synthetic (seeded: X Student-t4 unit var, W N(0,0.02), dY N(0,1e-4))",
+        "config": {"workload": WORKLOAD, "tokens": T, "d_in": D_IN, "d_out": D_OUT, "route": "mxfp4",
+                   "flags": "X col H32, W 2D32, dY row SR + col H32", "out_dtype": "f32",
+                   "l2": "inputs larger than L2 (419 MB bf16 per step)", "parallelism": f"replicas{world}"},
+        "tokens_per_s": round(T / (ms * 1e-3) * world, 1),
+        "quant_gbs": round(quant_gbs, 1),
+        "kernels": kernels,
+        "roofline": roof,
+        "e2e": None if args.no_e2e else {
+            "value": round(flops_per_step() / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 6,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "input_gen_s": round(gen_s, 1),
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+# ------------------------------------------------------------ CPU oracle ----
+_CPU_T = {}
+
+
+def _cpu_tensors():
+    if not _CPU_T:
+        from synthetic import config_tensors
+        _CPU_T.update(config_tensors("c2_mx_w1"))
+    return _CPU_T
+
+
+def cpu_sample_once(tiles: int = 1, seed: int = 1):
+    """One bounded sample of the workload on the CPU oracle: quantize the
+    operand slices that `tiles` 128 x 128 output tiles of each contraction need
+    and contract them.  Returns (flops counted, seconds)."""
+    import oracle
+    t = _cpu_tensors()
+    x, w, dy, s = t["x"], t["w"], t["dy"], t["signs"]
+    rng = np.random.default_rng(seed)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for _ in range(tiles):
+        mt = int(rng.integers(0, T // 128)) * 128
+        ot = int(rng.integers(0, D_OUT // 128)) * 128
+        it = int(rng.integers(0, D_IN // 128)) * 128
+        # Fprop tile: rows mt of X, rows ot of W
+        a = oracle.quantize(np.ascontiguousarray(x[mt:mt + 128]), "mx", "row")
+        b = oracle.quantize(np.ascontiguousarray(w[ot:ot + 128]), "mx", "row", weight2d=True)
+        oracle.gemm(a, b)
+        # Dgrad tile: rows mt of dY (SR), columns it of W
+        a = oracle.quantize(np.ascontiguousarray(dy[mt:mt + 128]), "mx", "row", sr=True, seed=1)
+        b = oracle.quantize(np.ascontiguousarray(w[:, it:it + 128]), "mx", "col", weight2d=True)
+        oracle.gemm(a, b)
+        # Wgrad tile: columns ot of dY, columns it of X (both H32)
+        a = oracle.quantize(np.ascontiguousarray(dy[:, ot:ot + 128]), "mx", "col", hadamard=True, signs=s)
+        b = oracle.quantize(np.ascontiguousarray(x[:, it:it + 128]), "mx", "col", hadamard=True, signs=s)
+        oracle.gemm(a, b)
+        flops += 2.0 * 128 * 128 * (D_IN + D_OUT + T)
+    return flops, time.perf_counter() - t0
+
+
+def cpu_baseline_sample(seconds_target: float = 10.0) -> dict:
+    flops, secs = 0.0, 0.0
+    n = 0
+    while secs < seconds_target or n == 0:
+        f, s = cpu_sample_once(1, seed=100 + n)
+        flops += f
+        secs += s
+        n += 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} x (one 128x128 output tile of each of Fprop, Dgrad, Wgrad at the full K, with the "
+                      f"quantization of the operand slices it needs), single-threaded C oracle, {secs:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    for i in range(args.warmup):
+        cpu_sample_once(1, seed=i)
+    flops, secs = 0.0, 0.0
+    for i in range(args.steps):
+        f, s = cpu_sample_once(1, seed=1000 + i)
+        flops += f
+        secs += s
+    v = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded tensors as the GPU arm)",
+        "config": {"workload": WORKLOAD, "tokens": T, "d_in": D_IN, "d_out": D_OUT, "route": "mxfp4"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": "per step: one 128x128 output tile of each of Fprop, Dgrad, Wgrad at the full K "
+                                   "plus the quantization of the operand slices it needs (single-threaded C oracle)"},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="token count (default 8192); smaller values make a profiling-sized case")
+    args = ap.parse_args()
+    if args.tokens:
+        global T
+        T = int(args.tokens)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

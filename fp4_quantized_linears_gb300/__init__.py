@@ -101,6 +101,13 @@ def _declare(L):
         "fp4_linear_fprop": (ctypes.c_int, [tp, tp, vp, ctypes.c_int, ctypes.c_float, vp]),
         "fp4_linear_dgrad": (ctypes.c_int, [tp, tp, vp, ctypes.c_int, ctypes.c_float, vp]),
         "fp4_linear_wgrad": (ctypes.c_int, [tp, tp, vp, ctypes.c_float, vp]),
+        "fp4_residual_rmsnorm_fwd": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint, vp, vp, vp, c_i64, c_i64, c_i64,
+                                                    ctypes.c_float, vp, vp, tp, tp, vp, vp, c_sz, vp]),
+        "fp4_residual_rmsnorm_bwd": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint, ctypes.c_int, vp, vp, vp, vp, vp,
+                                                    c_i64, c_i64, c_u64, c_u64, vp, tp, tp, vp, c_sz, vp]),
+        "fp4_rmsnorm_bwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int, c_i64, c_i64, ctypes.POINTER(c_sz)]),
+        "fp4_swiglu_fwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, tp, tp, vp, vp]),
+        "fp4_swiglu_bwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, c_u64, c_u64, tp, tp, vp, vp, vp]),
         "fp4_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_int)]),
         "fp4_status_reset": (ctypes.c_int, [vp]),
     }
@@ -243,6 +250,135 @@ def fp4_linear_wgrad(dy_col: QView, x_col: QView, dw: torch.Tensor | None = None
     _check(load().fp4_linear_wgrad(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(dw.data_ptr()), beta,
                                    _stream(stream)), "fp4_linear_wgrad")
     return dw
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _views(route, R, C, views, flags, device, row_out, col_out):
+    if views & FP4_VIEW_ROW and row_out is None:
+        row_out = alloc_view(route, R, C, flags, device)
+    if views & FP4_VIEW_COL and col_out is None:
+        col_out = alloc_view(route, C, R, flags, device)
+    return row_out, col_out
+
+
+def _sync_fields(v, st):
+    if st is not None:
+        v.rows, v.cols, v.route, v.outer_count = st.rows, st.cols, st.route, st.outer_count
+
+
+def fp4_residual_rmsnorm_fwd(r: torch.Tensor, b: torch.Tensor | None, g: torch.Tensor, route, views: int = 3,
+                             eps: float = 1e-5, r_out=None, rstd=None, y_row=None, y_col=None, y_tap=None,
+                             workspace=None, stream=None):
+    """r' = bf16(r + b), rstd, and the FP4 views of y = bf16(r' * rstd * g).
+
+    Returns (r_out, rstd, y_row, y_col)."""
+    rt = _route(route)
+    R, C = r.shape
+    dev = r.device
+    r_out = torch.empty((R, C), dtype=torch.bfloat16, device=dev) if r_out is None else r_out
+    rstd = torch.empty(R, dtype=torch.float32, device=dev) if rstd is None else rstd
+    y_row, y_col = _views(rt, R, C, views, 0, dev, y_row, y_col)
+    need = fp4_quantize_workspace_bytes(rt, R, C, views, 0)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    rs = y_row.struct() if y_row is not None else None
+    cs = y_col.struct() if y_col is not None else None
+    _check(load().fp4_residual_rmsnorm_fwd(rt, views, _ptr(r), _ptr(b), _ptr(g), R, C, r.stride(0), eps, _ptr(r_out),
+                                           _ptr(rstd), ctypes.byref(rs) if rs else None,
+                                           ctypes.byref(cs) if cs else None, _ptr(y_tap), _ptr(workspace),
+                                           workspace.numel() if workspace is not None else 0, _stream(stream)),
+           "fp4_residual_rmsnorm_fwd")
+    _sync_fields(y_row, rs)
+    _sync_fields(y_col, cs)
+    return r_out, rstd, y_row, y_col
+
+
+def fp4_rmsnorm_bwd_workspace_bytes(route, rows: int, cols: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fp4_rmsnorm_bwd_workspace_bytes(_route(route), rows, cols, ctypes.byref(n)),
+           "fp4_rmsnorm_bwd_workspace_bytes")
+    return n.value
+
+
+def fp4_residual_rmsnorm_bwd(dy: torch.Tensor, r_prime: torch.Tensor, rstd: torch.Tensor, g: torch.Tensor,
+                             dres: torch.Tensor | None, route, views: int = 3, sr: bool = True, sr_seed: int = 0,
+                             sr_offset: int = 0, dr=None, dr_row=None, dr_col=None, workspace=None, stream=None):
+    """dr = bf16(RMSNorm backward(dy) + dres) and its FP4 views (row view SR).
+
+    Returns (dr, dr_row, dr_col)."""
+    rt = _route(route)
+    R, C = dy.shape
+    dev = dy.device
+    dr = torch.empty((R, C), dtype=torch.bfloat16, device=dev) if dr is None else dr
+    flags = FP4_FLAG_SR_ROW if sr else 0
+    dr_row, dr_col = _views(rt, R, C, views, flags, dev, dr_row, dr_col)
+    if workspace is None:
+        workspace = torch.empty(fp4_rmsnorm_bwd_workspace_bytes(rt, R, C), dtype=torch.uint8, device=dev)
+    rs = dr_row.struct() if dr_row is not None else None
+    cs = dr_col.struct() if dr_col is not None else None
+    _check(load().fp4_residual_rmsnorm_bwd(rt, views, int(sr), _ptr(dy), _ptr(r_prime), _ptr(rstd), _ptr(g),
+                                           _ptr(dres), R, C, sr_seed, sr_offset, _ptr(dr),
+                                           ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None,
+                                           _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp4_residual_rmsnorm_bwd")
+    _sync_fields(dr_row, rs)
+    _sync_fields(dr_col, cs)
+    return dr, dr_row, dr_col
+
+
+def fp4_swiglu_fwd(x_row: QView, w13_row: QView, f: int, a1=None, a3=None, h_row=None, h_col=None, h_tap=None,
+                   quantize: bool = True, stream=None):
+    """Fused W1/W3 contraction + SiLU gate.  Returns (a1, a3, h_row, h_col).
+
+    For MXFP4 the FP4 views of h are emitted (unless quantize=False, then
+    h_tap must be given); for NVFP4 h_tap is required and views are None."""
+    T = x_row.rows
+    dev = x_row.codes.device
+    a1 = torch.empty((T, f), dtype=torch.bfloat16, device=dev) if a1 is None else a1
+    a3 = torch.empty((T, f), dtype=torch.bfloat16, device=dev) if a3 is None else a3
+    mx = x_row.route == FP4_ROUTE_MXFP4
+    if mx and quantize:
+        h_row = alloc_view(FP4_ROUTE_MXFP4, T, f, 0, dev) if h_row is None else h_row
+        h_col = alloc_view(FP4_ROUTE_MXFP4, f, T, 0, dev) if h_col is None else h_col
+    else:
+        h_row = h_col = None
+    a, b = x_row.struct(), w13_row.struct()
+    rs = h_row.struct() if h_row is not None else None
+    cs = h_col.struct() if h_col is not None else None
+    _check(load().fp4_swiglu_fwd(ctypes.byref(a), ctypes.byref(b), f, _ptr(a1), _ptr(a3),
+                                 ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None, _ptr(h_tap),
+                                 _stream(stream)), "fp4_swiglu_fwd")
+    if rs:
+        _sync_fields(h_row, rs)
+        _sync_fields(h_col, cs)
+    return a1, a3, h_row, h_col
+
+
+def fp4_swiglu_bwd(dy2_row: QView, w2_col: QView, f: int, a1: torch.Tensor, a3: torch.Tensor, sr_seed: int = 0,
+                   sr_offset: int = 0, da13_row=None, da13_col=None, dh_tap=None, da13_tap=None,
+                   quantize: bool = True, stream=None):
+    """Fused W2 Dgrad + SiLU derivative.  Returns (da13_row, da13_col)."""
+    T = dy2_row.rows
+    dev = dy2_row.codes.device
+    mx = dy2_row.route == FP4_ROUTE_MXFP4
+    if mx and quantize:
+        da13_row = alloc_view(FP4_ROUTE_MXFP4, T, 2 * f, 0, dev) if da13_row is None else da13_row
+        da13_col = alloc_view(FP4_ROUTE_MXFP4, 2 * f, T, 0, dev) if da13_col is None else da13_col
+    else:
+        da13_row = da13_col = None
+    a, b = dy2_row.struct(), w2_col.struct()
+    rs = da13_row.struct() if da13_row is not None else None
+    cs = da13_col.struct() if da13_col is not None else None
+    _check(load().fp4_swiglu_bwd(ctypes.byref(a), ctypes.byref(b), f, _ptr(a1), _ptr(a3), sr_seed, sr_offset,
+                                 ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None, _ptr(dh_tap),
+                                 _ptr(da13_tap), _stream(stream)), "fp4_swiglu_bwd")
+    if rs:
+        _sync_fields(da13_row, rs)
+        _sync_fields(da13_col, cs)
+    return da13_row, da13_col
 
 
 def fp4_status(stream=None) -> int:

@@ -67,9 +67,12 @@ int fp4_quantize_workspace_bytes(int route, int64_t rows, int64_t cols, unsigned
     return FP4_OK;
 }
 
-int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int route, unsigned views, unsigned flags,
-                 uint64_t sr_seed, uint64_t sr_offset, const int8_t* hadamard_signs, fp4_tensor* row_out,
-                 fp4_tensor* col_out, void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
+// Validate a quantizer call and fill its parameters; nothing is enqueued.
+// x may be NULL when the caller produces it in an earlier kernel (pre-ops).
+static int prepare_quant(const void* x, bool x_from_pre, int64_t rows, int64_t cols, int64_t ld, int route,
+                         unsigned views, unsigned flags, uint64_t sr_seed, uint64_t sr_offset,
+                         const int8_t* hadamard_signs, fp4_tensor* row_out, fp4_tensor* col_out, void* workspace,
+                         size_t workspace_bytes, QuantParams* p) {
     if (!route_ok(route)) return FP4_ERR_INVALID_ARG;
     if ((views & ~3u) || views == 0 || (flags & ~7u)) return FP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0 || ld < cols) return FP4_ERR_INVALID_ARG;
@@ -79,7 +82,6 @@ int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int rout
     if ((flags & FP4_FLAG_HADAMARD_COL) && route != FP4_ROUTE_MXFP4) return FP4_ERR_ROUTE_MISMATCH;
     const bool do_row = views & FP4_VIEW_ROW, do_col = views & FP4_VIEW_COL;
     if ((do_row && !row_out) || (do_col && !col_out)) return FP4_ERR_INVALID_ARG;
-    const int32_t oc_row = outer_count_of(route, rows, flags), oc_col = outer_count_of(route, cols, flags);
     for (int v = 0; v < 2; ++v) {
         fp4_tensor* t = v == 0 ? (do_row ? row_out : nullptr) : (do_col ? col_out : nullptr);
         if (!t) continue;
@@ -97,45 +99,120 @@ int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int rout
     size_t need = 0;
     fp4_quantize_workspace_bytes(route, rows, cols, views, flags, &need);
     if (need > 0 && (!workspace || workspace_bytes < need)) return FP4_ERR_WORKSPACE;
-    if (rows > 0 && cols > 0 && (!x || !aligned16(x) || ld % 8)) return FP4_ERR_INVALID_ARG;
+    if (rows > 0 && cols > 0 && !x_from_pre && (!x || !aligned16(x) || ld % 8)) return FP4_ERR_INVALID_ARG;
 
     if (do_row) {
         row_out->rows = rows;
         row_out->cols = cols;
         row_out->route = route;
-        row_out->outer_count = oc_row;
+        row_out->outer_count = outer_count_of(route, rows, flags);
     }
     if (do_col) {
         col_out->rows = cols;
         col_out->cols = rows;
         col_out->route = route;
-        col_out->outer_count = oc_col;
+        col_out->outer_count = outer_count_of(route, cols, flags);
     }
-    if (rows == 0 || cols == 0) return FP4_OK;
-
-    QuantParams p{};
-    p.x = static_cast<const uint16_t*>(x);
-    p.R = rows;
-    p.C = cols;
-    p.ld = ld;
-    p.route = route;
-    p.views = views;
-    p.flags = flags;
-    p.seed = sr_seed;
-    p.offset = sr_offset;
-    p.sign_mask = sign_mask;
+    *p = QuantParams{};
+    p->x = static_cast<const uint16_t*>(x);
+    p->R = rows;
+    p->C = cols;
+    p->ld = ld;
+    p->route = route;
+    p->views = views;
+    p->flags = flags;
+    p->seed = sr_seed;
+    p->offset = sr_offset;
+    p->sign_mask = sign_mask;
     if (do_row) {
-        p.row_codes = static_cast<uint8_t*>(row_out->codes);
-        p.row_scales = static_cast<uint8_t*>(row_out->scales);
-        p.row_outer = row_out->outer;
+        p->row_codes = static_cast<uint8_t*>(row_out->codes);
+        p->row_scales = static_cast<uint8_t*>(row_out->scales);
+        p->row_outer = row_out->outer;
     }
     if (do_col) {
-        p.col_codes = static_cast<uint8_t*>(col_out->codes);
-        p.col_scales = static_cast<uint8_t*>(col_out->scales);
-        p.col_outer = col_out->outer;
+        p->col_codes = static_cast<uint8_t*>(col_out->codes);
+        p->col_scales = static_cast<uint8_t*>(col_out->scales);
+        p->col_outer = col_out->outer;
     }
-    p.amax_ws = static_cast<uint32_t*>(workspace);
+    p->amax_ws = static_cast<uint32_t*>(workspace);
+    return FP4_OK;
+}
+
+int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int route, unsigned views, unsigned flags,
+                 uint64_t sr_seed, uint64_t sr_offset, const int8_t* hadamard_signs, fp4_tensor* row_out,
+                 fp4_tensor* col_out, void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
+    QuantParams p;
+    int rc = prepare_quant(x, false, rows, cols, ld, route, views, flags, sr_seed, sr_offset, hadamard_signs, row_out,
+                           col_out, workspace, workspace_bytes, &p);
+    if (rc != FP4_OK || rows == 0 || cols == 0) return rc;
     return launch_quantize(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp4_residual_rmsnorm_fwd(int route, unsigned views, const void* r, const void* b, const void* g, int64_t rows,
+                             int64_t cols, int64_t ld, float eps, void* r_out, float* rstd, fp4_tensor* y_row,
+                             fp4_tensor* y_col, void* y_tap, void* workspace, size_t workspace_bytes,
+                             fp4_stream_t stream) {
+    QuantParams p;
+    int rc = prepare_quant(r_out, true, rows, cols, cols, route, views, 0, 0, 0, nullptr, y_row, y_col, workspace,
+                           workspace_bytes, &p);
+    if (rc != FP4_OK || rows == 0 || cols == 0) return rc;
+    if (ld < cols || ld % 8) return FP4_ERR_INVALID_ARG;
+    if (!r || !g || !r_out || !rstd || !aligned16(r) || !aligned16(g) || !aligned16(r_out) || (b && !aligned16(b)) ||
+        (y_tap && !aligned16(y_tap)))
+        return FP4_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f)) return FP4_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rc = launch_rmsnorm_fwd_stats(static_cast<const uint16_t*>(r), static_cast<const uint16_t*>(b), rows, cols, ld,
+                                  eps, static_cast<uint16_t*>(r_out), rstd, s);
+    if (rc != FP4_OK) return rc;
+    p.pre = PRE_RMSNORM_FWD;
+    p.rstd = rstd;
+    p.g = static_cast<const uint16_t*>(g);
+    p.tap = static_cast<uint16_t*>(y_tap);
+    return launch_quantize(p, s);
+}
+
+int fp4_rmsnorm_bwd_workspace_bytes(int route, int64_t rows, int64_t cols, size_t* bytes) {
+    if (!bytes) return FP4_ERR_INVALID_ARG;
+    size_t q = 0;
+    int rc = fp4_quantize_workspace_bytes(route, rows, cols, 3, 0, &q);
+    if (rc != FP4_OK) return rc;
+    size_t stats = ((size_t)rows * 4 + 255) / 256 * 256;
+    *bytes = stats + q;
+    return FP4_OK;
+}
+
+int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, const void* r_prime,
+                             const float* rstd, const void* g, const void* dres, int64_t rows, int64_t cols,
+                             uint64_t sr_seed, uint64_t sr_offset, void* dr, fp4_tensor* dr_row, fp4_tensor* dr_col,
+                             void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
+    if (!route_ok(route) || rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;
+    if (rows % 128 || cols % 128) return FP4_ERR_UNSUPPORTED_SHAPE;
+    size_t need = 0;
+    fp4_rmsnorm_bwd_workspace_bytes(route, rows, cols, &need);
+    const size_t stats = ((size_t)rows * 4 + 255) / 256 * 256;
+    if (rows > 0 && cols > 0 && (!workspace || workspace_bytes < need)) return FP4_ERR_WORKSPACE;
+    void* qws = workspace ? static_cast<uint8_t*>(workspace) + stats : nullptr;
+    QuantParams p;
+    int rc = prepare_quant(dy, false, rows, cols, cols, route, views, sr ? FP4_FLAG_SR_ROW : 0, sr_seed, sr_offset,
+                           nullptr, dr_row, dr_col, qws, workspace ? workspace_bytes - stats : 0, &p);
+    if (rc != FP4_OK || rows == 0 || cols == 0) return rc;
+    if (!r_prime || !rstd || !g || !dr || !aligned16(r_prime) || !aligned16(g) || !aligned16(dr) ||
+        (dres && !aligned16(dres)))
+        return FP4_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float* mean_g = static_cast<float*>(workspace);
+    rc = launch_rmsnorm_bwd_stats(static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(r_prime), rstd,
+                                  static_cast<const uint16_t*>(g), rows, cols, mean_g, s);
+    if (rc != FP4_OK) return rc;
+    p.pre = PRE_RMSNORM_BWD;
+    p.rstd = rstd;
+    p.g = static_cast<const uint16_t*>(g);
+    p.mean_g = mean_g;
+    p.rp = static_cast<const uint16_t*>(r_prime);
+    p.dres = static_cast<const uint16_t*>(dres);
+    p.tap = static_cast<uint16_t*>(dr);
+    return launch_quantize(p, s);
 }
 
 static int linear(const fp4_tensor* a, const fp4_tensor* b, void* c, int out_dtype, float beta, fp4_stream_t stream) {
@@ -171,6 +248,125 @@ static int linear(const fp4_tensor* a, const fp4_tensor* b, void* c, int out_dty
     g.c = c;
     g.out_dtype = out_dtype;
     g.beta = beta;
+    return launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static bool view_ok(const fp4_tensor* t) {
+    return t && t->codes && t->scales && aligned16(t->codes) && aligned16(t->scales);
+}
+
+static void set_view(fp4_tensor* t, int64_t rows, int64_t cols, int route) {
+    t->rows = rows;
+    t->cols = cols;
+    t->route = route;
+    t->outer_count = 0;
+}
+
+static void fill_operands(GemmParams& g, const fp4_tensor* a, const fp4_tensor* b) {
+    const bool nv = a->route != FP4_ROUTE_MXFP4;
+    g.a_codes = static_cast<const uint8_t*>(a->codes);
+    g.a_scales = static_cast<const uint8_t*>(a->scales);
+    g.a_outer = nv ? a->outer : nullptr;
+    g.a_outer_count = a->outer_count;
+    g.b_codes = static_cast<const uint8_t*>(b->codes);
+    g.b_scales = static_cast<const uint8_t*>(b->scales);
+    g.b_outer = nv ? b->outer : nullptr;
+    g.b_outer_count = b->outer_count;
+    g.nv = nv ? 1 : 0;
+}
+
+static int check_operand(const fp4_tensor* t) {
+    if (!t || !route_ok(t->route)) return FP4_ERR_INVALID_ARG;
+    if (!view_ok(t)) return FP4_ERR_INVALID_ARG;
+    if (t->route != FP4_ROUTE_MXFP4 && (!t->outer || (t->outer_count != 1 && t->outer_count != t->rows / 128)))
+        return FP4_ERR_INVALID_ARG;
+    return FP4_OK;
+}
+
+int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f, void* a1, void* a3,
+                   fp4_tensor* h_row, fp4_tensor* h_col, void* h_tap, fp4_stream_t stream) {
+    int rc;
+    if ((rc = check_operand(x_row)) != FP4_OK || (rc = check_operand(w13_row)) != FP4_OK) return rc;
+    if (x_row->route != w13_row->route) return FP4_ERR_ROUTE_MISMATCH;
+    const int64_t T = x_row->rows, d = x_row->cols;
+    if (f <= 0 || w13_row->rows != 2 * f || w13_row->cols != d) return FP4_ERR_UNSUPPORTED_SHAPE;
+    if (T % 128 || f % 128 || d % 256 || T <= 0) return FP4_ERR_UNSUPPORTED_SHAPE;
+    if (!a1 || !a3 || !aligned16(a1) || !aligned16(a3) || (h_tap && !aligned16(h_tap))) return FP4_ERR_INVALID_ARG;
+    const bool mx = x_row->route == FP4_ROUTE_MXFP4;
+    if (w13_row->route != FP4_ROUTE_MXFP4 && w13_row->outer_count != 1) return FP4_ERR_INVALID_ARG;
+    if (mx) {
+        if ((h_row == nullptr) != (h_col == nullptr)) return FP4_ERR_INVALID_ARG;
+        if (h_row && (!view_ok(h_row) || !view_ok(h_col))) return FP4_ERR_INVALID_ARG;
+        if (!h_row && !h_tap) return FP4_ERR_INVALID_ARG;
+    } else {
+        if (h_row || h_col) return FP4_ERR_ROUTE_MISMATCH;
+        if (!h_tap) return FP4_ERR_INVALID_ARG;
+    }
+    GemmParams g{};
+    fill_operands(g, x_row, w13_row);
+    g.M = T;
+    g.N = f;
+    g.K = d;
+    g.epi = 1;
+    g.f = f;
+    g.a1 = static_cast<uint16_t*>(a1);
+    g.a3 = static_cast<uint16_t*>(a3);
+    g.tap0 = static_cast<uint16_t*>(h_tap);
+    if (mx && h_row) {
+        g.quantize = 1;
+        g.q_row_codes = static_cast<uint8_t*>(h_row->codes);
+        g.q_row_scales = static_cast<uint8_t*>(h_row->scales);
+        g.q_col_codes = static_cast<uint8_t*>(h_col->codes);
+        g.q_col_scales = static_cast<uint8_t*>(h_col->scales);
+        set_view(h_row, T, f, FP4_ROUTE_MXFP4);
+        set_view(h_col, f, T, FP4_ROUTE_MXFP4);
+    }
+    return launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp4_swiglu_bwd(const fp4_tensor* dy2_row, const fp4_tensor* w2_col, int64_t f, const void* a1, const void* a3,
+                   uint64_t sr_seed, uint64_t sr_offset, fp4_tensor* da13_row, fp4_tensor* da13_col, void* dh_tap,
+                   void* da13_tap, fp4_stream_t stream) {
+    int rc;
+    if ((rc = check_operand(dy2_row)) != FP4_OK || (rc = check_operand(w2_col)) != FP4_OK) return rc;
+    if (dy2_row->route != w2_col->route) return FP4_ERR_ROUTE_MISMATCH;
+    const int64_t T = dy2_row->rows, d = dy2_row->cols;
+    if (f <= 0 || w2_col->rows != f || w2_col->cols != d) return FP4_ERR_UNSUPPORTED_SHAPE;
+    if (T % 128 || f % 128 || d % 256 || T <= 0) return FP4_ERR_UNSUPPORTED_SHAPE;
+    if (!a1 || !a3 || !aligned16(a1) || !aligned16(a3) || (dh_tap && !aligned16(dh_tap)) ||
+        (da13_tap && !aligned16(da13_tap)))
+        return FP4_ERR_INVALID_ARG;
+    const bool mx = dy2_row->route == FP4_ROUTE_MXFP4;
+    if (mx) {
+        if ((da13_row == nullptr) != (da13_col == nullptr)) return FP4_ERR_INVALID_ARG;
+        if (da13_row && (!view_ok(da13_row) || !view_ok(da13_col))) return FP4_ERR_INVALID_ARG;
+        if (!da13_row && !da13_tap) return FP4_ERR_INVALID_ARG;
+    } else {
+        if (da13_row || da13_col) return FP4_ERR_ROUTE_MISMATCH;
+        if (!da13_tap) return FP4_ERR_INVALID_ARG;
+    }
+    GemmParams g{};
+    fill_operands(g, dy2_row, w2_col);
+    g.M = T;
+    g.N = f;
+    g.K = d;
+    g.epi = 2;
+    g.f = f;
+    g.a1 = const_cast<uint16_t*>(static_cast<const uint16_t*>(a1));
+    g.a3 = const_cast<uint16_t*>(static_cast<const uint16_t*>(a3));
+    g.tap0 = static_cast<uint16_t*>(dh_tap);
+    g.tap1 = static_cast<uint16_t*>(da13_tap);
+    g.seed = sr_seed;
+    g.offset = sr_offset;
+    if (mx && da13_row) {
+        g.quantize = 1;
+        g.q_row_codes = static_cast<uint8_t*>(da13_row->codes);
+        g.q_row_scales = static_cast<uint8_t*>(da13_row->scales);
+        g.q_col_codes = static_cast<uint8_t*>(da13_col->codes);
+        g.q_col_scales = static_cast<uint8_t*>(da13_col->scales);
+        set_view(da13_row, T, 2 * f, FP4_ROUTE_MXFP4);
+        set_view(da13_col, 2 * f, T, FP4_ROUTE_MXFP4);
+    }
     return launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -49,19 +49,25 @@ FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
 
 // --------------------------------------------------------------- E2M1 SR ---
 // Adjacent-bin stochastic rounding (Sec. 2.5, Eq. 9): with q- <= |v| < q+
-// neighbouring grid values, round up iff u * 2^-16 < (|v| - q-) / (q+ - q-);
-// |v| >= 6 saturates.  All steps are exact in binary32.
+// neighbouring grid values, round up iff u * 2^-16 < p = (|v| - q-) / (q+ - q-);
+// |v| >= 6 saturates.  Evaluated exactly on the binary32 bits of |v|:
+//   |v| in [1, 6): the grid has one fraction bit, so q- is the value
+//     truncated to one fraction bit (index (bits >> 22) - 252) and
+//     p = (22 low fraction bits) / 2^22, i.e. up iff u << 6 < low22;
+//   |v| < 1: spacing 0.5, t = |v| * 2^17 (exact), q- index = (t >= 2^16),
+//     p * 2^16 = t - index * 2^16 (exact), up iff u < p * 2^16.
 FP4_DEV uint32_t e2m1_sr(float v, uint32_t u16) {
-    float a = fabsf(v);
-    uint32_t sign = (__float_as_uint(v) >> 31) << 3;
-    if (a >= 6.0f) return sign | 7u;
-    uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f);
-    // grid value of index lo and the reciprocal of the spacing to lo + 1
-    float qm = lo < 4 ? 0.5f * (float)lo : (lo == 4 ? 2.0f : (lo == 5 ? 3.0f : 4.0f));
-    float inv_sp = lo < 4 ? 2.0f : (lo < 6 ? 1.0f : 0.5f);
-    float p = __fmul_rn(__fsub_rn(a, qm), inv_sp);
-    uint32_t up = __fmul_rn((float)u16, 1.0f) < __fmul_rn(p, 65536.0f) ? 1u : 0u;
-    return sign | (lo + up);
+    const uint32_t bits = __float_as_uint(v);
+    const uint32_t a = bits & 0x7FFFFFFFu;
+    const uint32_t sign = (bits >> 28) & 8u;
+    const uint32_t hi_code = (a >> 22) - 252u + ((u16 << 6) < (a & 0x3FFFFFu) ? 1u : 0u);
+    const float t = __fmul_rn(__uint_as_float(a), 131072.0f);
+    const uint32_t lo_idx = t >= 65536.0f ? 1u : 0u;
+    const float tt = __fsub_rn(t, lo_idx ? 65536.0f : 0.0f);
+    const uint32_t lo_code = lo_idx + ((float)u16 < tt ? 1u : 0u);
+    uint32_t code = a >= 0x3F800000u ? hi_code : lo_code;
+    code = a >= 0x40C00000u ? 7u : code;  // |v| >= 6 saturates
+    return sign | code;
 }
 
 // --------------------------------------------------------------- E4M3 ------

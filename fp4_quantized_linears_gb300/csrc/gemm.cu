@@ -1,5 +1,5 @@
 // gemm.cu -- block-scaled FP4 GEMM on the 5th-generation tensor cores
-// (tcgen05) of sm_103a.
+// (tcgen05) of sm_103a, with the fused producer epilogues.
 //
 // Computes C[m][n] = alpha(m, n) * sum_k A_hat[m][k] B_hat[n][k] + beta * C[m][n]
 // for the three contractions of "Format-Aware Fusion for Fast FP4
@@ -9,17 +9,31 @@
 // the CTA-local epilogue of Sec. 2.2.2 (the factors stay fixed over the whole
 // K reduction and are applied together after it).
 //
-// Structure (one CTA per 128 x BN output tile, 192 threads):
-//   warp 0      TMA producer: 2D tensor loads of the A and B code tiles
-//               (128-byte swizzle) and 1D bulk copies of their scale atoms
-//               into a STAGES-deep shared-memory ring guarded by mbarriers;
-//   warp 1      allocates tensor memory; one thread copies each stage's scale
-//               atoms into TMEM (tcgen05.cp 32x128b.warpx4) and issues the
-//               block-scaled MMAs (kind::mxf4 with E8M0 scales, 2 per 64 K, or
-//               kind::mxf4nvf4 with E4M3 scales, 4 per 64 K) into a 128 x BN
-//               FP32 accumulator in TMEM; tcgen05.commit releases each stage;
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (each warp its own
-//               32-lane quarter), alpha / beta, 16-byte global stores.
+// The same mainloop serves the gated-FFN boundary of Sec. 3.2:
+//   EPI_SWIGLU_FWD  B tile = 128 rows of W1 + the matching 128 rows of W3, so
+//                   one accumulator holds a1 and a3 of the same outputs; the
+//                   epilogue writes the retained BF16 a1, a3 and emits
+//                   h = SiLU(a1) * a3 directly as the FP4 row- and
+//                   column-facing inputs of the W2 contractions;
+//   EPI_SWIGLU_BWD  the W2 Dgrad accumulator dh is combined with the SiLU
+//                   derivative (reading the retained a1, a3) and emitted as the
+//                   FP4 views of [da1 | da3] for the W1/W3 Dgrad (row view,
+//                   stochastic rounding) and Wgrad (column view).
+//
+// Structure: a persistent kernel, one CTA per SM (320 threads), clusters of
+// CM CTAs along M that share the B tile through TMA multicast:
+//   warp 0      TMA producer: A tile (128 rows), this CTA's share of the B
+//               tile multicast to the cluster, scale atoms (1D bulk copies),
+//               into a STAGES-deep ring of mbarrier-guarded stages;
+//   warp 1      owns the TMEM allocation; one thread copies each stage's
+//               scale atoms into TMEM (tcgen05.cp 32x128b.warpx4) and issues
+//               the block-scaled MMAs (kind::mxf4 E8M0 / kind::mxf4nvf4 E4M3)
+//               into a 128 x BN FP32 accumulator; the stage is released to
+//               every CTA of the cluster by a multicast tcgen05.commit;
+//   warps 2-9   epilogue: drain the accumulator from TMEM into registers
+//               (each warp one lane quarter x one column half), release it so
+//               the next tile's MMAs start, then finish and store the tile
+//               while the tensor core runs the next one.
 // Every mbarrier wait is bounded: a wait that runs out sets the sticky status
 // word to FP4_ERR_TIMEOUT, the roles drain what they issued and the CTA
 // returns, releasing its tensor memory.
@@ -41,16 +55,26 @@ __device__ unsigned int g_status_gemm;
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 256;          // FP4 elements per stage (128 bytes per row)
+constexpr int BK = 256;  // FP4 elements per stage (128 bytes per row)
 constexpr int BK_BYTES = BK / 2;
-constexpr int STAGES = 4;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
+constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 512;
-constexpr int SF_COL0 = 256;     // first TMEM column of the scale-factor region
+constexpr int SF_COL0 = 256;  // first TMEM column of the scale-factor region
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+constexpr int GROUP_M = 8;     // raster: 8 M-units per band
 
 // ------------------------------------------------------------ PTX wrappers -
 FP4_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+FP4_DEV uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+FP4_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 FP4_DEV void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
@@ -58,6 +82,9 @@ FP4_DEV void mbar_init(uint64_t* bar, uint32_t count) {
 FP4_DEV void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+FP4_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 FP4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
@@ -72,6 +99,7 @@ FP4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait; false (and the status word set) when the budget runs out.
 FP4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
     long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (clock64() - t0 > WAIT_CYCLES) {
@@ -89,6 +117,15 @@ FP4_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64
         "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// The same box delivered to the same offset in every CTA of `mask`, each
+// completing bytes on its own barrier at the same offset.
+FP4_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
 FP4_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -102,6 +139,13 @@ FP4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;"
 FP4_DEV void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+FP4_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 // shared-memory matrix descriptor (tcgen05): start, LBO, SBO (bytes >> 4),
@@ -145,19 +189,91 @@ FP4_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// 32 lanes x 32 columns of 32-bit accumulator; the wait is part of the same
+// asm statement, so no use of the registers can be scheduled before it.
 FP4_DEV void tmem_ld32(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        : "r"(taddr)
+        : "memory");
+}
+
+
+// ------------------------------------------------------ epilogue helpers --
+constexpr int ST_LDS = 136;  // staging row stride (bf16 elements)
+
+FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
+
+// MX row/column block of 32 values: scale byte and 16 bytes of RN codes.
+FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
+    uint32_t am = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
+    const int e = e8m0_exponent_up(am);
+    const float mult = exp2_neg(e);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            int i = q * 8 + b * 2;
+            word |= e2m1x2_rn(__fmul_rn(v[i], mult), __fmul_rn(v[i + 1], mult)) << (8 * b);
+        }
+        w[q] = word;
+    }
+    packed = make_uint4(w[0], w[1], w[2], w[3]);
+    return (uint32_t)(e + 127);
+}
+
+// MX block of 32 values with stochastic rounding (logical indices 8*g0 ..).
+FP4_DEV uint32_t mx_block_sr(const float* v, uint64_t g0, uint64_t seed, uint64_t offset, uint4& packed) {
+    uint32_t am = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
+    const int e = e8m0_exponent_up(am);
+    const float mult = exp2_neg(e);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 rb = sr_bits8(g0 + q, seed, offset);
+        uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            int i = q * 8 + b * 2;
+            uint32_t c0 = e2m1_sr(__fmul_rn(v[i], mult), rw[b] & 0xFFFFu);
+            uint32_t c1 = e2m1_sr(__fmul_rn(v[i + 1], mult), rw[b] >> 16);
+            word |= (c0 | (c1 << 4)) << (8 * b);
+        }
+        w[q] = word;
+    }
+    packed = make_uint4(w[0], w[1], w[2], w[3]);
+    return (uint32_t)(e + 127);
+}
+
+FP4_DEV void store_bf16x32(uint16_t* dst, const float* v) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = (uint32_t)f32_to_bf16_rn(v[i + 2 * j]) | ((uint32_t)f32_to_bf16_rn(v[i + 2 * j + 1]) << 16);
+        *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
 // ----------------------------------------------------------------- kernel -
+enum { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
+
 struct KParams {
     const uint8_t* a_scales;
     const uint8_t* b_scales;
@@ -168,39 +284,78 @@ struct KParams {
     void* c;
     int out_dtype;
     float beta;
+    // fused SwiGLU
+    int64_t f;             // inner width (W1/W3 rows); B rows of W3 start at f
+    uint16_t* a1;          // bf16 [M][f]: written (fwd) / read (bwd)
+    uint16_t* a3;
+    uint16_t* tap0;        // fwd: h;  bwd: dh            (bf16 [M][f], optional)
+    uint16_t* tap1;        // bwd: [da1 | da3]            (bf16 [M][2f], optional)
+    int quantize;          // emit the MX views below
+    uint8_t* q_row_codes;  // fwd: Q_r(h) [M][f];   bwd: Q_r(da13) [M][2f]
+    uint8_t* q_row_scales;
+    uint8_t* q_col_codes;  // fwd: Q_c(h) [f][M];   bwd: Q_c(da13) [2f][M]
+    uint8_t* q_col_scales;
+    uint64_t seed, offset;
 };
 
-template <bool NV, int BN>
+template <bool NV, int BN, int EPI>
 struct Cfg {
-    static constexpr int SF_CHUNKS = NV ? 4 : 2;           // 512-byte atoms per 128 rows per stage
-    static constexpr int A_BYTES = BM * BK_BYTES;          // 16 KB
-    static constexpr int B_BYTES = BN * BK_BYTES;          // 16 / 32 KB
+    static constexpr int STAGES = EPI == EPI_STORE ? 4 : (BN == 256 ? 3 : 4);
+    static constexpr int SF_CHUNKS = NV ? 4 : 2;  // 512-byte atoms per 128 rows per stage
+    static constexpr int A_BYTES = BM * BK_BYTES;
+    static constexpr int B_BYTES = BN * BK_BYTES;
     static constexpr int SFA_BYTES = SF_CHUNKS * 512;
     static constexpr int SFB_BYTES = (BN / 128) * SF_CHUNKS * 512;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr int SF_COLS_A = SF_CHUNKS * 4;          // TMEM columns per stage
+    static constexpr int SF_COLS_A = SF_CHUNKS * 4;
     static constexpr int SF_COLS_B = SF_CHUNKS * (BN / 32);
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int STAGING = EPI == EPI_STORE ? 0 : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + 256 /*barriers*/;
     static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <bool NV, int BN>
+template <bool NV, int BN, int EPI, int CM>
 __global__ void __launch_bounds__(THREADS, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, KParams p) {
-    using C = Cfg<NV, BN>;
+    using C = Cfg<NV, BN, EPI>;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+    uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::STAGING);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain_bar = acc_empty + 1;  // MMA completion point at the end
+    uint64_t* epi_bar = drain_bar + 1;    // bounded barrier among the epilogue warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+    const uint32_t rank = CM > 1 ? cluster_rank() : 0;
     const int num_kb = (int)(p.K / BK);
+    const int64_t m_units = p.M / (BM * CM);
+    const int64_t n_blocks = EPI == EPI_SWIGLU_FWD ? p.f / 128 : p.N / BN;
+    const int64_t n_units = m_units * n_blocks;
+    const int64_t cluster_id = blockIdx.x / CM, n_clusters = gridDim.x / CM;
+
+    auto unit_coords = [&](int64_t u, int64_t& m0, int64_t& n0) {
+        const int64_t per_group = (int64_t)GROUP_M * n_blocks;
+        const int64_t g = u / per_group, within = u % per_group;
+        const int64_t m_first = g * GROUP_M;
+        const int64_t gs = min((int64_t)GROUP_M, m_units - m_first);
+        const int64_t mu = m_first + within % gs;
+        const int64_t nb = within / gs;
+        m0 = (mu * CM + rank) * BM;
+        n0 = nb * (EPI == EPI_SWIGLU_FWD ? 128 : BN);
+    };
+    // global row of B where 128-row half h of the tile starts
+    auto b_row = [&](int64_t n0, int h) -> int64_t {
+        return EPI == EPI_SWIGLU_FWD ? h * p.f + n0 : n0 + 128 * h;
+    };
 
     auto stage_a = [&](int s) { return smem + s * C::STAGE_BYTES; };
     auto stage_b = [&](int s) { return smem + s * C::STAGE_BYTES + C::A_BYTES; };
@@ -210,9 +365,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], CM);
         }
         mbar_init(acc_full, 1);
+        mbar_init(acc_empty, EPI_WARPS);
+        mbar_init(drain_bar, 1);
+        mbar_init(epi_bar, EPI_WARPS * 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -222,135 +380,372 @@ __global__ void __launch_bounds__(THREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+    }
     tc_fence_before();
     __syncthreads();
+    if (CM > 1) cluster_sync();  // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer ----
-        const int64_t k_atoms_a = NV ? p.K / 64 : p.K / 128;  // atoms per 128-row block
-        int last_issued = -1;
-        for (int kb = 0; kb < num_kb; ++kb) {
-            int s = kb % STAGES;
-            if (kb >= STAGES) {
-                if (*abort_flag || !mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1)) {
+        const int64_t k_atoms = NV ? p.K / 64 : p.K / 128;  // scale atoms per 128-row block
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int64_t u = cluster_id; u < n_units && ok; u += n_clusters) {
+            int64_t m0, n0;
+            unit_coords(u, m0, n0);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) {
                     *abort_flag = 1;
+                    ok = false;
                     break;
                 }
-            }
-            mbar_expect_tx(&full[s], C::STAGE_BYTES);
-            tma_load_2d(stage_a(s), &tmA, kb * BK_BYTES, (int)m0, &full[s]);
-            tma_load_2d(stage_b(s), &tmB, kb * BK_BYTES, (int)n0, &full[s]);
-            const uint8_t* sfa = p.a_scales + ((m0 >> 7) * k_atoms_a + (int64_t)kb * C::SF_CHUNKS) * 512;
-            bulk_load(stage_sfa(s), sfa, C::SFA_BYTES, &full[s]);
+                mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+                tma_load_2d(stage_a(stage), &tmA, kb * BK_BYTES, (int)m0, &full[stage]);
+                if (CM > 1) {
+                    // this CTA's 128-row share of B, delivered to the whole cluster
+                    for (int h = (int)rank; h < BN / 128; h += CM)
+                        tma_load_2d_mc(stage_b(stage) + h * 128 * BK_BYTES, &tmB, kb * BK_BYTES, (int)b_row(n0, h),
+                                       &full[stage], (uint16_t)((1u << CM) - 1));
+                } else {
+                    for (int h = 0; h < BN / 128; ++h)
+                        tma_load_2d(stage_b(stage) + h * 128 * BK_BYTES, &tmB, kb * BK_BYTES, (int)b_row(n0, h),
+                                    &full[stage]);
+                }
+                const uint8_t* sfa = p.a_scales + ((m0 >> 7) * k_atoms + (int64_t)kb * C::SF_CHUNKS) * 512;
+                bulk_load(stage_sfa(stage), sfa, C::SFA_BYTES, &full[stage]);
 #pragma unroll
-            for (int h = 0; h < BN / 128; ++h) {
-                const uint8_t* sfb = p.b_scales + (((n0 >> 7) + h) * k_atoms_a + (int64_t)kb * C::SF_CHUNKS) * 512;
-                bulk_load(stage_sfb(s) + h * C::SF_CHUNKS * 512, sfb, C::SF_CHUNKS * 512, &full[s]);
+                for (int h = 0; h < BN / 128; ++h) {
+                    const uint8_t* sfb =
+                        p.b_scales + ((b_row(n0, h) >> 7) * k_atoms + (int64_t)kb * C::SF_CHUNKS) * 512;
+                    bulk_load(stage_sfb(stage) + h * C::SF_CHUNKS * 512, sfb, C::SF_CHUNKS * 512, &full[stage]);
+                }
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
             }
-            last_issued = kb;
         }
-        if (*abort_flag) {
-            // drain: wait (bounded) for the loads still in flight
-            for (int kb = last_issued - STAGES + 1; kb <= last_issued; ++kb)
-                if (kb >= 0) mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1);
+        if (!ok) {
+            // drain: wait (bounded) for the loads of the stages still in flight
+            int s = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < STAGES && i < issued; ++i) {
+                if (--s < 0) {
+                    s = STAGES - 1;
+                    ph ^= 1;
+                }
+                mbar_wait(&full[s], ph);
+            }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer ------
         const uint32_t sf_base = tmem + SF_COL0;
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-            int s = kb % STAGES;
-            if (*abort_flag || !mbar_wait(&full[s], (kb / STAGES) & 1)) {
+        for (int64_t u = cluster_id; u < n_units && ok; u += n_clusters) {
+            if (*abort_flag || !mbar_wait(acc_empty, acc_phase ^ 1)) {
                 *abort_flag = 1;
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sfa_col = sf_base + s * C::SF_COLS;
-            const uint32_t sfb_col = sfa_col + C::SF_COLS_A;
-            // scale atoms -> TMEM (replicated into the four lane quarters)
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (*abort_flag || !mbar_wait(&full[stage], phase)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sfa_col = sf_base + stage * C::SF_COLS;
+                const uint32_t sfb_col = sfa_col + C::SF_COLS_A;
 #pragma unroll
-            for (int c = 0; c < C::SF_CHUNKS; ++c) {
-                tc_cp_sf(sfa_col + 4 * c, smem_desc(smem_u32(stage_sfa(s) + c * 512), 0, 128, LAYOUT_NONE));
+                for (int c = 0; c < C::SF_CHUNKS; ++c) {
+                    tc_cp_sf(sfa_col + 4 * c, smem_desc(smem_u32(stage_sfa(stage) + c * 512), 0, 128, LAYOUT_NONE));
 #pragma unroll
-                for (int h = 0; h < BN / 128; ++h)
-                    tc_cp_sf(sfb_col + c * (BN / 32) + 4 * h,
-                             smem_desc(smem_u32(stage_sfb(s) + (h * C::SF_CHUNKS + c) * 512), 0, 128, LAYOUT_NONE));
-            }
-            const uint32_t a_base = smem_u32(stage_a(s)), b_base = smem_u32(stage_b(s));
+                    for (int h = 0; h < BN / 128; ++h)
+                        tc_cp_sf(sfb_col + c * (BN / 32) + 4 * h,
+                                 smem_desc(smem_u32(stage_sfb(stage) + (h * C::SF_CHUNKS + c) * 512), 0, 128,
+                                           LAYOUT_NONE));
+                }
+                const uint32_t a_base = smem_u32(stage_a(stage)), b_base = smem_u32(stage_b(stage));
 #pragma unroll
-            for (int kk = 0; kk < BK / 64; ++kk) {
-                uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
-                uint64_t bd = smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
-                uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                if (NV) {
-                    uint32_t id = make_idesc(BN, false, 0, 0);
-                    mma_nvf4(tmem, ad, bd, id, sfa_col + 4 * kk, sfb_col + kk * (BN / 32), acc);
-                } else {
-                    int c = kk >> 1;
-                    uint32_t sid = (uint32_t)(kk & 1) * 2;
-                    uint32_t id = make_idesc(BN, true, sid, sid);
-                    mma_mxf4(tmem, ad, bd, id, sfa_col + 4 * c, sfb_col + c * (BN / 32), acc);
+                for (int kk = 0; kk < BK / 64; ++kk) {
+                    uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
+                    uint64_t bd = smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
+                    uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    if (NV) {
+                        mma_nvf4(tmem, ad, bd, make_idesc(BN, false, 0, 0), sfa_col + 4 * kk, sfb_col + kk * (BN / 32),
+                                 acc);
+                    } else {
+                        const int c = kk >> 1;
+                        const uint32_t sid = (uint32_t)(kk & 1) * 2;
+                        mma_mxf4(tmem, ad, bd, make_idesc(BN, true, sid, sid), sfa_col + 4 * c,
+                                 sfb_col + c * (BN / 32), acc);
+                    }
+                }
+                if (CM > 1)
+                    tc_commit_mc(&empty[stage], (uint16_t)((1u << CM) - 1));
+                else
+                    tc_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
                 }
             }
-            tc_commit(&empty[s]);
+            if (!ok) break;
+            tc_commit(acc_full);
+            acc_phase ^= 1;
         }
-        tc_commit(acc_full);  // also the drain point of everything issued
-        if (!ok) mbar_wait(acc_full, 0);
+        // drain point of everything issued (its own barrier, so that no
+        // epilogue wait on acc_full can see an extra phase)
+        tc_commit(drain_bar);
+        mbar_wait(drain_bar, 0);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue --------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const bool ok = mbar_wait(acc_full, 0) && !*abort_flag;
-        if (!ok) *abort_flag = 1;
-        tc_fence_after();
-        if (ok) {
-            const int64_t m = m0 + q * 32 + lane;
-            float sa = 1.0f;
-            if (NV) sa = __fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]);
-#pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + cc * 32, r);
-                const int64_t n = n0 + cc * 32;
-                float alpha = 1.0f;
-                if (NV) alpha = __fmul_rn(sa, __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n >> 7)]));
-                if (p.out_dtype == FP4_OUT_F32) {
-                    float* dst = reinterpret_cast<float*>(p.c) + m * p.N + n;
+        const int q = warp & 3;               // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;     // column half
+        const int lr = q * 32 + lane;         // row within the tile
+        const int et = (warp - 2) * 32 + lane;  // epilogue thread index 0..255
+        uint32_t acc_phase = 0, epi_phase = 0;
+        bool epi_ok = true;
+        // bounded barrier among the 256 epilogue threads
+        auto epi_sync = [&]() {
+            mbar_arrive(epi_bar);
+            if (!mbar_wait(epi_bar, epi_phase)) {
+                *abort_flag = 1;
+                epi_ok = false;
+            }
+            epi_phase ^= 1;
+        };
+        for (int64_t u = cluster_id; u < n_units && epi_ok; u += n_clusters) {
+            int64_t m0, n0;
+            unit_coords(u, m0, n0);
+            if (!mbar_wait(acc_full, acc_phase)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int64_t m = m0 + lr;
+            const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+            if constexpr (EPI == EPI_STORE) {
+                constexpr int NC = BN / 64;  // 32-column chunks per thread
+                uint32_t r[NC * 32];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        float4 v = make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
-                                               __uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
-                        if (p.beta != 0.0f) {
-                            float4 o = *reinterpret_cast<const float4*>(dst + i);
-                            v.x += p.beta * o.x; v.y += p.beta * o.y; v.z += p.beta * o.z; v.w += p.beta * o.w;
-                        }
-                        *reinterpret_cast<float4*>(dst + i) = v;
-                    }
-                } else {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.c) + m * p.N + n;
+                for (int c = 0; c < NC; ++c) tmem_ld32(lane_base + half * (BN / 2) + 32 * c, r + 32 * c);
+                tc_fence_before();
+                if (lane == 0) mbar_arrive(acc_empty);
+                float sa = 1.0f;
+                if (NV) sa = __fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]);
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint32_t w[4];
+                for (int c = 0; c < NC; ++c) {
+                    const int64_t n = n0 + half * (BN / 2) + 32 * c;
+                    float alpha = 1.0f;
+                    if (NV) alpha = __fmul_rn(sa, __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n >> 7)]));
+                    const uint32_t* rc = r + 32 * c;
+                    if (p.out_dtype == FP4_OUT_F32) {
+                        float* dst = reinterpret_cast<float*>(p.c) + m * p.N + n;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            float x0 = __uint_as_float(r[i + 2 * j]) * alpha;
-                            float x1 = __uint_as_float(r[i + 2 * j + 1]) * alpha;
+                        for (int i = 0; i < 32; i += 4) {
+                            float4 v = make_float4(__uint_as_float(rc[i]) * alpha, __uint_as_float(rc[i + 1]) * alpha,
+                                                   __uint_as_float(rc[i + 2]) * alpha,
+                                                   __uint_as_float(rc[i + 3]) * alpha);
                             if (p.beta != 0.0f) {
-                                x0 += p.beta * bf16_to_f32(dst[i + 2 * j]);
-                                x1 += p.beta * bf16_to_f32(dst[i + 2 * j + 1]);
+                                float4 o = *reinterpret_cast<const float4*>(dst + i);
+                                v.x += p.beta * o.x;
+                                v.y += p.beta * o.y;
+                                v.z += p.beta * o.z;
+                                v.w += p.beta * o.w;
                             }
-                            w[j] = (uint32_t)f32_to_bf16_rn(x0) | ((uint32_t)f32_to_bf16_rn(x1) << 16);
+                            *reinterpret_cast<float4*>(dst + i) = v;
                         }
-                        *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
+                    } else {
+                        uint16_t* dst = reinterpret_cast<uint16_t*>(p.c) + m * p.N + n;
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            v[i] = __uint_as_float(rc[i]) * alpha;
+                            if (p.beta != 0.0f) v[i] += p.beta * bf16_to_f32(dst[i]);
+                        }
+                        store_bf16x32(dst, v);
                     }
                 }
+            } else if constexpr (EPI == EPI_SWIGLU_FWD) {
+                // output columns [64*half, 64*half + 64) of this 128-wide tile:
+                // a1 in accumulator columns 0..127, a3 in 128..255
+                uint32_t r1[64], r3[64];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(lane_base + 64 * half + 32 * c, r1 + 32 * c);
+                    tmem_ld32(lane_base + 128 + 64 * half + 32 * c, r3 + 32 * c);
+                }
+                tc_fence_before();
+                if (lane == 0) mbar_arrive(acc_empty);
+                uint16_t* hs = reinterpret_cast<uint16_t*>(staging);
+                uint8_t* row_atom = staging + BM * ST_LDS * 2;
+                uint8_t* col_atom = row_atom + 512;
+                float alpha = 1.0f;
+                if (NV)
+                    alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
+                                      __fdiv_rn(1.0f, p.b_outer[0]));
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    const int oc = 64 * half + 32 * c;
+                    const int64_t n = n0 + oc;
+                    float h[32], x1[32], x3[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        x1[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r1[32 * c + i]) * alpha));
+                        x3[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r3[32 * c + i]) * alpha));
+                        const float s = __fdiv_rn(x1[i], __fadd_rn(1.0f, expf(-x1[i])));
+                        h[i] = bf16_to_f32(f32_to_bf16_rn(__fmul_rn(s, x3[i])));
+                    }
+                    store_bf16x32(p.a1 + m * p.f + n, x1);
+                    store_bf16x32(p.a3 + m * p.f + n, x3);
+                    if (p.tap0) store_bf16x32(p.tap0 + m * p.f + n, h);
+                    if (p.quantize) {
+                        uint4 pk;
+                        uint32_t sc = mx_block_rn(h, pk);
+                        *reinterpret_cast<uint4*>(p.q_row_codes + m * (p.f >> 1) + (n >> 1)) = pk;
+                        row_atom[atom_off(lr, oc >> 5)] = (uint8_t)sc;
+                        store_bf16x32(hs + lr * ST_LDS + oc, h);
+                    }
+                }
+                if (p.quantize) {
+                    epi_sync();
+                    if (!epi_ok) break;
+                    // column-facing view: stored row = output column, blocks along the tokens
+#pragma unroll 1
+                    for (int k = 0; k < 2; ++k) {
+                        const int idx = et + 256 * k, j = idx >> 7, cidx = idx & 127;
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = bf16_to_f32(hs[(32 * j + i) * ST_LDS + cidx]);
+                        uint4 pk;
+                        uint32_t sc = mx_block_rn(v, pk);
+                        *reinterpret_cast<uint4*>(p.q_col_codes + (n0 + cidx) * (p.M >> 1) + ((m0 + 32 * j) >> 1)) =
+                            pk;
+                        col_atom[atom_off(cidx, j)] = (uint8_t)sc;
+                    }
+                    epi_sync();
+                    if (!epi_ok) break;
+                    if (et < 32) {
+                        const int64_t a = (m0 >> 7) * (p.f >> 7) + (n0 >> 7);
+                        *reinterpret_cast<uint4*>(p.q_row_scales + a * 512 + et * 16) =
+                            *reinterpret_cast<const uint4*>(row_atom + et * 16);
+                    } else if (et < 64) {
+                        const int64_t a = (n0 >> 7) * (p.M >> 7) + (m0 >> 7);
+                        *reinterpret_cast<uint4*>(p.q_col_scales + a * 512 + (et - 32) * 16) =
+                            *reinterpret_cast<const uint4*>(col_atom + (et - 32) * 16);
+                    }
+                    epi_sync();
+                }
+            } else {
+                // EPI_SWIGLU_BWD: dh for output columns [64*half, 64*half + 64)
+                uint32_t r[64];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + 64 * half + 32 * c, r + 32 * c);
+                tc_fence_before();
+                if (lane == 0) mbar_arrive(acc_empty);
+                uint16_t* s1 = reinterpret_cast<uint16_t*>(staging);
+                uint16_t* s3 = s1 + BM * ST_LDS;
+                uint8_t* atoms = staging + 2 * BM * ST_LDS * 2;  // row da1, row da3, col da1, col da3
+                float alpha = 1.0f;
+                if (NV)
+                    alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
+                                      __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n0 >> 7)]));
+                const int64_t f2 = 2 * p.f;
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    const int oc = 64 * half + 32 * c;
+                    const int64_t n = n0 + oc;
+                    float d1[32], d3[32];
+                    {
+                        float dh[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            dh[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r[32 * c + i]) * alpha));
+                        if (p.tap0) store_bf16x32(p.tap0 + m * p.f + n, dh);
+                        const uint16_t* pa1 = p.a1 + m * p.f + n;
+                        const uint16_t* pa3 = p.a3 + m * p.f + n;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) {
+                            uint4 v1 = *reinterpret_cast<const uint4*>(pa1 + i);
+                            uint4 v3 = *reinterpret_cast<const uint4*>(pa3 + i);
+                            uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float x = (j & 1) ? bf16_hi(w1[j >> 1]) : bf16_lo(w1[j >> 1]);
+                                const float y = (j & 1) ? bf16_hi(w3[j >> 1]) : bf16_lo(w3[j >> 1]);
+                                const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
+                                const float g = dh[i + j];
+                                const float dsilu = sg * (1.0f + x * (1.0f - sg));
+                                d1[i + j] = bf16_to_f32(f32_to_bf16_rn(g * y * dsilu));
+                                d3[i + j] = bf16_to_f32(f32_to_bf16_rn(g * (x * sg)));
+                            }
+                        }
+                    }
+                    if (p.tap1) {
+                        store_bf16x32(p.tap1 + m * f2 + n, d1);
+                        store_bf16x32(p.tap1 + m * f2 + p.f + n, d3);
+                    }
+                    if (p.quantize) {
+                        uint4 pk;
+                        uint32_t sc = mx_block_sr(d1, (uint64_t)(m * f2 + n) >> 3, p.seed, p.offset, pk);
+                        *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + (n >> 1)) = pk;
+                        atoms[atom_off(lr, oc >> 5)] = (uint8_t)sc;
+                        sc = mx_block_sr(d3, (uint64_t)(m * f2 + p.f + n) >> 3, p.seed, p.offset, pk);
+                        *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + ((p.f + n) >> 1)) = pk;
+                        atoms[512 + atom_off(lr, oc >> 5)] = (uint8_t)sc;
+                        store_bf16x32(s1 + lr * ST_LDS + oc, d1);
+                        store_bf16x32(s3 + lr * ST_LDS + oc, d3);
+                    }
+                }
+                if (p.quantize) {
+                    epi_sync();
+                    if (!epi_ok) break;
+#pragma unroll 1
+                    for (int k = 0; k < 4; ++k) {
+                        const int idx = et + 256 * k, which = idx >> 9, j = (idx >> 7) & 3, cidx = idx & 127;
+                        const uint16_t* src = which ? s3 : s1;
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = bf16_to_f32(src[(32 * j + i) * ST_LDS + cidx]);
+                        uint4 pk;
+                        uint32_t sc = mx_block_rn(v, pk);
+                        const int64_t srow = (which ? p.f : 0) + n0 + cidx;
+                        *reinterpret_cast<uint4*>(p.q_col_codes + srow * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pk;
+                        atoms[1024 + which * 512 + atom_off(cidx, j)] = (uint8_t)sc;
+                    }
+                    epi_sync();
+                    if (!epi_ok) break;
+                    if (et < 128) {
+                        const int which = et >> 5, part = et & 31;
+                        int64_t a;
+                        if (which < 2)  // row views of da1 / da3 in [M][2f]
+                            a = (m0 >> 7) * (f2 >> 7) + ((which ? p.f : 0) + n0) / 128;
+                        else  // column views in [2f][M]
+                            a = (((which == 3 ? p.f : 0) + n0) >> 7) * (p.M >> 7) + (m0 >> 7);
+                        uint8_t* dst = (which < 2 ? p.q_row_scales : p.q_col_scales) + a * 512 + part * 16;
+                        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(atoms + which * 512 + part * 16);
+                    }
+                    epi_sync();
+                }
             }
+            acc_phase ^= 1;
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (CM > 1) cluster_sync();  // no peer still multicasts into this CTA
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
@@ -373,11 +768,11 @@ bool get_encode() {
     return g_encode != nullptr;
 }
 
-// K-major FP4 codes [rows][K/2] bytes as a 2D uint8 tensor, box 128 B x box_rows.
-bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K, int box_rows) {
+// K-major FP4 codes [rows][K/2] bytes as a 2D uint8 tensor, box 128 B x 128 rows.
+bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K) {
     cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, 128u};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -385,12 +780,61 @@ bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K, int 
     return r == CUDA_SUCCESS;
 }
 
-template <bool NV, int BN>
-int launch_t(const GemmParams& g, cudaStream_t stream) {
-    using C = Cfg<NV, BN>;
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64) dev = 63;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+template <bool NV, int BN, int EPI, int CM>
+int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream_t stream) {
+    using C = Cfg<NV, BN, EPI>;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, g.a_codes, g.M, g.K, BM) || !make_map(&tb, g.b_codes, g.N, g.K, BN)) return FP4_ERR_CUDA;
-    KParams p;
+    if (!make_map(&ta, g.a_codes, g.M, g.K) || !make_map(&tb, g.b_codes, g.b_rows, g.K)) return FP4_ERR_CUDA;
+    auto kern = fp4_gemm_kernel<NV, BN, EPI, CM>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool attr_done[64] = {};
+    if (dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return FP4_ERR_CUDA;
+        if (CM > 1 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+            return FP4_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    int max_clusters = sm_count() / CM;
+    if (CM > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CM;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3((unsigned)(max_clusters * CM));
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, (void*)kern, &cfg) == cudaSuccess && active > 0)
+            max_clusters = active;
+    }
+    const int64_t clusters = n_units < max_clusters ? n_units : max_clusters;
+    cfg.gridDim = dim3((unsigned)(clusters * CM));
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, kp) != cudaSuccess) return FP4_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
+KParams kparams_of(const GemmParams& g) {
+    KParams p{};
     p.a_scales = g.a_scales;
     p.b_scales = g.b_scales;
     p.a_outer = g.a_outer;
@@ -403,27 +847,56 @@ int launch_t(const GemmParams& g, cudaStream_t stream) {
     p.c = g.c;
     p.out_dtype = g.out_dtype;
     p.beta = g.beta;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    static bool attr_done[64] = {};
-    if (dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(fp4_gemm_kernel<NV, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-            cudaSuccess)
-            return FP4_ERR_CUDA;
-        attr_done[dev] = true;
-    }
-    dim3 grid((unsigned)(g.N / BN), (unsigned)(g.M / BM));
-    fp4_gemm_kernel<NV, BN><<<grid, THREADS, C::SMEM, stream>>>(ta, tb, p);
-    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+    p.f = g.f;
+    p.a1 = g.a1;
+    p.a3 = g.a3;
+    p.tap0 = g.tap0;
+    p.tap1 = g.tap1;
+    p.quantize = g.quantize;
+    p.q_row_codes = g.q_row_codes;
+    p.q_row_scales = g.q_row_scales;
+    p.q_col_codes = g.q_col_codes;
+    p.q_col_scales = g.q_col_scales;
+    p.seed = g.seed;
+    p.offset = g.offset;
+    return p;
 }
 
 }  // namespace
 
-int launch_gemm(const GemmParams& g, cudaStream_t stream) {
+int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     if (!get_encode()) return FP4_ERR_CUDA;
+    GemmParams g = g0;
+    const bool pair = (g.M / BM) % 2 == 0;
+    const KParams kp = kparams_of(g);
+    if (g.epi == 1) {  // SwiGLU forward: B = [W1; W3] with 2f rows, output width f
+        g.b_rows = 2 * g.f;
+        const int64_t units_1 = (g.M / BM) * (g.f / 128);
+        if (g.nv) return pair ? launch_t<true, 256, EPI_SWIGLU_FWD, 2>(g, kp, units_1 / 2, stream)
+                              : launch_t<true, 256, EPI_SWIGLU_FWD, 1>(g, kp, units_1, stream);
+        return pair ? launch_t<false, 256, EPI_SWIGLU_FWD, 2>(g, kp, units_1 / 2, stream)
+                    : launch_t<false, 256, EPI_SWIGLU_FWD, 1>(g, kp, units_1, stream);
+    }
+    g.b_rows = g.N;
+    if (g.epi == 2) {  // SwiGLU backward: W2 Dgrad, output [M][f]
+        const int64_t units_1 = (g.M / BM) * (g.N / 128);
+        if (g.nv) return pair ? launch_t<true, 128, EPI_SWIGLU_BWD, 2>(g, kp, units_1 / 2, stream)
+                              : launch_t<true, 128, EPI_SWIGLU_BWD, 1>(g, kp, units_1, stream);
+        return pair ? launch_t<false, 128, EPI_SWIGLU_BWD, 2>(g, kp, units_1 / 2, stream)
+                    : launch_t<false, 128, EPI_SWIGLU_BWD, 1>(g, kp, units_1, stream);
+    }
     const bool wide = (g.N % 256) == 0;
-    if (g.nv) return wide ? launch_t<true, 256>(g, stream) : launch_t<true, 128>(g, stream);
-    return wide ? launch_t<false, 256>(g, stream) : launch_t<false, 128>(g, stream);
+    const int64_t units_1 = (g.M / BM) * (g.N / (wide ? 256 : 128));
+    if (g.nv) {
+        if (wide) return pair ? launch_t<true, 256, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+                              : launch_t<true, 256, EPI_STORE, 1>(g, kp, units_1, stream);
+        return pair ? launch_t<true, 128, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+                    : launch_t<true, 128, EPI_STORE, 1>(g, kp, units_1, stream);
+    }
+    if (wide) return pair ? launch_t<false, 256, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+                          : launch_t<false, 256, EPI_STORE, 1>(g, kp, units_1, stream);
+    return pair ? launch_t<false, 128, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+                : launch_t<false, 128, EPI_STORE, 1>(g, kp, units_1, stream);
 }
 
 int gemm_status(cudaStream_t stream, int* code, bool reset) {

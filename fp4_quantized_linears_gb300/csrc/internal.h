@@ -23,7 +23,26 @@ struct QuantParams {
     uint8_t* col_scales;
     float* col_outer;
     uint32_t* amax_ws;  // NVFP4: [1 + R/128 + C/128] amax bit slots
+    // Optional element-wise pre-op applied while the tile is loaded (the
+    // residual-RMSNorm producer, Sec. 3.2):
+    //   PRE_RMSNORM_FWD  x = r',  value = bf16(fl32(fl32(r' * rstd[r]) * g[c]))
+    //   PRE_RMSNORM_BWD  x = dy,  value = bf16(fl32(fl32(rstd[r] * fl32(fl32(dy * g[c])
+    //                                 - fl32(fl32(r' * rstd[r]) * mean_g[r]))) + dres))
+    int pre;
+    const float* rstd;
+    const uint16_t* g;
+    const float* mean_g;
+    const uint16_t* rp;    // r' (bwd)
+    const uint16_t* dres;  // incoming residual gradient (bwd), may be NULL
+    uint16_t* tap;         // bf16 [R][C] copy of the values quantized (NULL: not written)
 };
+
+enum { PRE_NONE = 0, PRE_RMSNORM_FWD = 1, PRE_RMSNORM_BWD = 2 };
+
+int launch_rmsnorm_fwd_stats(const uint16_t* r, const uint16_t* b, int64_t R, int64_t C, int64_t ld, float eps,
+                             uint16_t* r_out, float* rstd, cudaStream_t stream);
+int launch_rmsnorm_bwd_stats(const uint16_t* dy, const uint16_t* rp, const float* rstd, const uint16_t* g, int64_t R,
+                             int64_t C, float* mean_g, cudaStream_t stream);
 
 int launch_quantize(const QuantParams& p, cudaStream_t stream);
 int quant_status(cudaStream_t stream, int* code, bool reset);
@@ -43,6 +62,20 @@ struct GemmParams {
     void* c;
     int out_dtype;  // FP4_OUT_F32 / FP4_OUT_BF16
     float beta;
+    // fused producer epilogues (0 = plain store, 1 = SwiGLU forward, 2 = SwiGLU backward)
+    int epi;
+    int64_t b_rows;       // rows of the B code tensor (set by the launcher)
+    int64_t f;            // SwiGLU inner width
+    uint16_t* a1;         // bf16 [M][f]
+    uint16_t* a3;
+    uint16_t* tap0;       // fwd h / bwd dh, bf16 [M][f], optional
+    uint16_t* tap1;       // bwd [da1 | da3], bf16 [M][2f], optional
+    int quantize;         // MX views emitted by the epilogue
+    uint8_t* q_row_codes;
+    uint8_t* q_row_scales;
+    uint8_t* q_col_codes;
+    uint8_t* q_col_scales;
+    uint64_t seed, offset;
 };
 
 int launch_gemm(const GemmParams& p, cudaStream_t stream);

@@ -63,25 +63,21 @@ FP4_DEV uint32_t amax_bits16(const float* v) {
     for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
     return m;
 }
-
-// Pack 32 E2M1 codes (RN) of v * mult into 16 bytes.
-FP4_DEV uint4 pack_rn32(const float* v, float mult) {
-    uint32_t w[4];
+// Packed per-half maximum of |bf16| over n bf16x2 words (bits of the low and
+// high halves' maxima in the two 16-bit lanes).
+template <int N>
+FP4_DEV uint32_t amax_words(const uint32_t* w) {
+    uint32_t m = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            int i = q * 8 + b * 2;
-            word |= e2m1x2_rn(__fmul_rn(v[i], mult), __fmul_rn(v[i + 1], mult)) << (8 * b);
-        }
-        w[q] = word;
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < N; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+    return m;
 }
+// fp32 bit pattern of a bf16 magnitude held in a 16-bit lane.
+FP4_DEV uint32_t lane_lo_f32bits(uint32_t m2) { return m2 << 16; }
+FP4_DEV uint32_t lane_hi_f32bits(uint32_t m2) { return m2 & 0xFFFF0000u; }
 
-// Two 16-blocks with their own multipliers.
-FP4_DEV uint4 pack_rn16x2(const float* v, float m0, float m1) {
+// Pack 32 E2M1 codes (RN) of v * m (m0 for values 0..15, m1 for 16..31).
+FP4_DEV uint4 pack_rn32(const float* v, float m0, float m1) {
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -118,10 +114,10 @@ FP4_DEV uint4 pack_sr32(const float* v, float m0, float m1, uint64_t g0, uint64_
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Fixed-sign H32 on 32 registers: signs, butterflies of stride 1..16, 1/sqrt(32).
-FP4_DEV void hadamard32(float* v, uint32_t neg_mask) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((neg_mask >> (i & 15)) & 1u) << 31));
+// H32 butterflies on 32 registers whose fixed signs were already applied:
+// stages of stride 1, 2, 4, 8 within each 16-value half, then the cross-half
+// stage of stride 16, then the binary32 multiply by fl32(1/sqrt(32)).
+FP4_DEV void hadamard32_nosign(float* v) {
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -138,45 +134,82 @@ FP4_DEV void hadamard32(float* v, uint32_t neg_mask) {
     for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], s);
 }
 
+// Load the 128x128 tile at (r0, c0) into shared memory (row stride LDS),
+// applying the pre-op; with write_tap the pre-op results are also stored.
+FP4_DEV void load_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* tile, bool write_tap) {
+    const int t = threadIdx.x;
+#pragma unroll 2
+    for (int i = 0; i < 8; ++i) {
+        int q = t + i * THREADS;
+        int rr = q >> 4, cc = (q & 15) * 8;
+        const int64_t gr = r0 + rr, gc = c0 + cc;
+        uint4 d = *reinterpret_cast<const uint4*>(p.x + gr * p.ld + gc);
+        if (p.pre != PRE_NONE) {
+            uint4 gv = *reinterpret_cast<const uint4*>(p.g + gc);
+            uint32_t xs[4] = {d.x, d.y, d.z, d.w}, gs[4] = {gv.x, gv.y, gv.z, gv.w}, os[4];
+            const float rs = p.rstd[gr];
+            if (p.pre == PRE_RMSNORM_FWD) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float y0 = __fmul_rn(__fmul_rn(bf16_lo(xs[k]), rs), bf16_lo(gs[k]));
+                    float y1 = __fmul_rn(__fmul_rn(bf16_hi(xs[k]), rs), bf16_hi(gs[k]));
+                    os[k] = (uint32_t)f32_to_bf16_rn(y0) | ((uint32_t)f32_to_bf16_rn(y1) << 16);
+                }
+            } else {
+                const float mg = p.mean_g[gr];
+                uint4 xv = *reinterpret_cast<const uint4*>(p.rp + gr * p.C + gc);
+                uint4 dv = p.dres ? *reinterpret_cast<const uint4*>(p.dres + gr * p.C + gc) : make_uint4(0, 0, 0, 0);
+                uint32_t rps[4] = {xv.x, xv.y, xv.z, xv.w}, drs[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float o[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float dyv = h ? bf16_hi(xs[k]) : bf16_lo(xs[k]);
+                        float gg = h ? bf16_hi(gs[k]) : bf16_lo(gs[k]);
+                        float xr = h ? bf16_hi(rps[k]) : bf16_lo(rps[k]);
+                        float dr = h ? bf16_hi(drs[k]) : bf16_lo(drs[k]);
+                        float xh = __fmul_rn(xr, rs);
+                        float gy = __fmul_rn(dyv, gg);
+                        float u = __fsub_rn(gy, __fmul_rn(xh, mg));
+                        o[h] = __fadd_rn(__fmul_rn(rs, u), dr);
+                    }
+                    os[k] = (uint32_t)f32_to_bf16_rn(o[0]) | ((uint32_t)f32_to_bf16_rn(o[1]) << 16);
+                }
+            }
+            d = make_uint4(os[0], os[1], os[2], os[3]);
+            if (write_tap && p.tap) *reinterpret_cast<uint4*>(p.tap + gr * p.C + gc) = d;
+        }
+        *reinterpret_cast<uint4*>(&tile[rr * LDS + cc]) = d;
+    }
+}
+
 FP4_DEV void check_finite(uint32_t amax_bits) {
     if (amax_bits >= 0x7F800000u) set_status(&g_status_quant, FP4_ERR_NONFINITE);
 }
 
-// Quantize one 32-value segment (MX: one block; NV: two blocks) and stage its
-// codes (16 B at code_dst) and scale bytes.
+// Scale choice of one 32-value segment (MX: one block; NV: two blocks of 16)
+// from the fp32 bit patterns of the blocks' amax; stages the scale bytes and
+// returns the two multipliers.
 template <bool NV>
-FP4_DEV void encode_segment(float* v, bool sr, uint64_t g0, const QuantParams& p, float senc, int fixed_e,
-                            uint32_t fixed_d0, uint32_t fixed_d1, float fixed_m0, float fixed_m1, bool fixed,
-                            uint8_t* code_dst, uint8_t* sc_base, int lr, int lj) {
-    uint4 packed;
+FP4_DEV void segment_scale(uint32_t am0, uint32_t am1, float senc, uint8_t* sc_base, int lr, int lj, float& m0,
+                           float& m1) {
     if (!NV) {
-        int e;
-        if (fixed) {
-            e = fixed_e;
-        } else {
-            uint32_t am = amax_bits32(v);
-            check_finite(am);
-            e = e8m0_exponent_up(am);
-        }
-        float mult = exp2_neg(e);
-        packed = sr ? pack_sr32(v, mult, mult, g0, p.seed, p.offset) : pack_rn32(v, mult);
+        check_finite(am0);
+        const int e = e8m0_exponent_up(am0);
+        m0 = m1 = exp2_neg(e);
         sc_base[atom_off(lr, lj)] = (uint8_t)(e + 127);
     } else {
-        uint32_t d0, d1;
-        float m0, m1;
-        if (fixed) {
-            d0 = fixed_d0; d1 = fixed_d1; m0 = fixed_m0; m1 = fixed_m1;
-        } else {
-            uint32_t a0 = amax_bits16(v), a1 = amax_bits16(v + 16);
-            check_finite(max(a0, a1));
-            d0 = nv_block_scale(__uint_as_float(a0), senc, m0);
-            d1 = nv_block_scale(__uint_as_float(a1), senc, m1);
-        }
-        packed = sr ? pack_sr32(v, m0, m1, g0, p.seed, p.offset) : pack_rn16x2(v, m0, m1);
-        sc_base[atom_off(lr, 2 * lj)] = (uint8_t)d0;
-        sc_base[atom_off(lr, 2 * lj + 1)] = (uint8_t)d1;
+        check_finite(max(am0, am1));
+        sc_base[atom_off(lr, 2 * lj)] = (uint8_t)nv_block_scale(__uint_as_float(am0), senc, m0);
+        sc_base[atom_off(lr, 2 * lj + 1)] = (uint8_t)nv_block_scale(__uint_as_float(am1), senc, m1);
     }
-    *reinterpret_cast<uint4*>(code_dst) = packed;
+}
+
+// Unpack the low (h = 0) or high (h = 1) bf16 lanes of 32 words into fp32.
+FP4_DEV void unpack_lane(const uint32_t* w, int h, float* v) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
 }
 
 template <bool NV>
@@ -188,14 +221,8 @@ __global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
     const bool w2d = (p.flags & FP4_FLAG_WEIGHT_2D) != 0;
     const bool do_row = (p.views & FP4_VIEW_ROW) != 0, do_col = (p.views & FP4_VIEW_COL) != 0;
 
-    // 1. tile -> shared memory (16-byte coalesced loads)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int q = t + i * THREADS;
-        int rr = q >> 4, cc = (q & 15) * 8;
-        uint4 d = *reinterpret_cast<const uint4*>(p.x + (r0 + rr) * p.ld + c0 + cc);
-        *reinterpret_cast<uint4*>(&s.tile[rr * LDS + cc]) = d;
-    }
+    // 1. tile -> shared memory (16-byte coalesced loads, optional pre-op)
+    load_tile(p, r0, c0, s.tile, true);
 
     // outer factors of this tile's row strip / column strip
     float senc_row = 1.0f, senc_col = 1.0f;
@@ -266,62 +293,105 @@ __global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
         const bool sr = (p.flags & FP4_FLAG_SR_ROW) != 0;
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {
-            int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
-            float v[32];
+            const int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
+            uint32_t w[16];
             const uint16_t* src = &s.tile[r * LDS + j * 32];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
-                uint32_t w[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    v[q * 8 + 2 * b] = bf16_lo(w[b]);
-                    v[q * 8 + 2 * b + 1] = bf16_hi(w[b]);
-                }
+                const uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
+                w[4 * q] = d.x; w[4 * q + 1] = d.y; w[4 * q + 2] = d.z; w[4 * q + 3] = d.w;
             }
-            uint64_t g0 = (uint64_t)(((r0 + r) * p.C + c0 + 32 * j) >> 3);
-            int fe = 0;
-            uint32_t d0 = 0, d1 = 0;
-            float m0 = 0.f, m1 = 0.f;
+            float m0, m1;
             if (w2d) {
                 if (!NV) {
-                    fe = s.tile_e[(r >> 5) * 4 + j];
+                    const int e = s.tile_e[(r >> 5) * 4 + j];
+                    m0 = m1 = exp2_neg(e);
+                    s.row_sc[atom_off(r, j)] = (uint8_t)(e + 127);
                 } else {
-                    int tl = (r >> 4) * 8 + 2 * j;
-                    d0 = s.tile_d[tl]; d1 = s.tile_d[tl + 1];
-                    m0 = s.tile_m[tl]; m1 = s.tile_m[tl + 1];
+                    const int tl = (r >> 4) * 8 + 2 * j;
+                    m0 = s.tile_m[tl];
+                    m1 = s.tile_m[tl + 1];
+                    s.row_sc[atom_off(r, 2 * j)] = (uint8_t)s.tile_d[tl];
+                    s.row_sc[atom_off(r, 2 * j + 1)] = (uint8_t)s.tile_d[tl + 1];
                 }
+            } else if (!NV) {
+                const uint32_t a2 = amax_words<16>(w);
+                segment_scale<false>(max(lane_lo_f32bits(a2), lane_hi_f32bits(a2)), 0, 0.f, s.row_sc, r, j, m0, m1);
+            } else {
+                const uint32_t a0 = amax_words<8>(w), a1 = amax_words<8>(w + 8);
+                segment_scale<true>(max(lane_lo_f32bits(a0), lane_hi_f32bits(a0)),
+                                    max(lane_lo_f32bits(a1), lane_hi_f32bits(a1)), senc_row, s.row_sc, r, j, m0, m1);
             }
-            encode_segment<NV>(v, sr, g0, p, senc_row, fe, d0, d1, m0, m1, w2d, &s.row_codes[r * 64 + j * 16],
-                               s.row_sc, r, j);
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                v[2 * i] = bf16_lo(w[i]);
+                v[2 * i + 1] = bf16_hi(w[i]);
+            }
+            uint4 packed;
+            if (sr) {
+                const uint64_t g0 = (uint64_t)(((r0 + r) * p.C + c0 + 32 * j) >> 3);
+                packed = pack_sr32(v, m0, m1, g0, p.seed, p.offset);
+            } else {
+                packed = pack_rn32(v, m0, m1);
+            }
+            *reinterpret_cast<uint4*>(&s.row_codes[r * 64 + j * 16]) = packed;
         }
     }
 
-    // 4. column-facing view: segment (c, j) = 32 values of local column c
-    //    starting at local row 32 j (stored row c, blocks along the rows)
+    // 4. column-facing view: thread = (column pair cp, row block j); the pair
+    //    (2 cp, 2 cp + 1) is read as 32 bf16x2 words down the tile, and each
+    //    column is one 32-value segment of its stored row (blocks along the rows)
     if (do_col) {
         const bool had = (p.flags & FP4_FLAG_HADAMARD_COL) != 0;
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
-            int idx = t + k * THREADS, j = idx >> 7, c = idx & 127;
-            float v[32];
+        const int cp = t & 63, j = t >> 6;
+        uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = bf16_to_f32(s.tile[(j * 32 + i) * LDS + c]);
-            if (had) hadamard32(v, p.sign_mask);
-            int fe = 0;
-            uint32_t d0 = 0, d1 = 0;
-            float m0 = 0.f, m1 = 0.f;
+        for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&s.tile[(j * 32 + i) * LDS + 2 * cp]);
+        if (had) {
+            // the sign of position i (mod 16) applies to both columns of the pair
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] ^= ((p.sign_mask >> (i & 15)) & 1u) * 0x80008000u;
+        }
+        uint32_t a_lo0 = 0, a_hi0 = 0, a_lo1 = 0, a_hi1 = 0;  // NV: [h][block]
+        if (!had && !w2d) {
+            if (!NV) {
+                const uint32_t a2 = amax_words<32>(w);
+                a_lo0 = lane_lo_f32bits(a2);
+                a_hi0 = lane_hi_f32bits(a2);
+            } else {
+                const uint32_t b0 = amax_words<16>(w), b1 = amax_words<16>(w + 16);
+                a_lo0 = lane_lo_f32bits(b0);
+                a_hi0 = lane_hi_f32bits(b0);
+                a_lo1 = lane_lo_f32bits(b1);
+                a_hi1 = lane_hi_f32bits(b1);
+            }
+        }
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * cp + h;
+            float v[32];
+            unpack_lane(w, h, v);
+            float m0, m1;
             if (w2d) {
                 if (!NV) {
-                    fe = s.tile_e[j * 4 + (c >> 5)];
+                    const int e = s.tile_e[j * 4 + (c >> 5)];
+                    m0 = m1 = exp2_neg(e);
+                    s.col_sc[atom_off(c, j)] = (uint8_t)(e + 127);
                 } else {
-                    int tl = (2 * j) * 8 + (c >> 4);
-                    d0 = s.tile_d[tl]; d1 = s.tile_d[tl + 8];
-                    m0 = s.tile_m[tl]; m1 = s.tile_m[tl + 8];
+                    const int tl = (2 * j) * 8 + (c >> 4);
+                    m0 = s.tile_m[tl];
+                    m1 = s.tile_m[tl + 8];
+                    s.col_sc[atom_off(c, 2 * j)] = (uint8_t)s.tile_d[tl];
+                    s.col_sc[atom_off(c, 2 * j + 1)] = (uint8_t)s.tile_d[tl + 8];
                 }
+            } else if (had) {
+                hadamard32_nosign(v);
+                segment_scale<NV>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
+            } else {
+                segment_scale<NV>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1);
             }
-            encode_segment<NV>(v, false, 0, p, senc_col, fe, d0, d1, m0, m1, w2d, &s.col_codes[c * 64 + j * 16],
-                               s.col_sc, c, j);
+            *reinterpret_cast<uint4*>(&s.col_codes[c * 64 + j * 16]) = pack_rn32(v, m0, m1);
         }
     }
     __syncthreads();
@@ -361,17 +431,25 @@ __global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
 
 // Tile-amax pre-pass for NVFP4: max |x| of each 128x128 tile folded into the
 // tensor slot ws[0], the tile's row-strip slot and its column-strip slot.
-__global__ void __launch_bounds__(THREADS) nv_amax_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t ld,
-                                                         uint32_t* ws, int64_t n_row_strips) {
+__global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
     __shared__ uint32_t red[THREADS / 32];
+    extern __shared__ __align__(16) uint8_t amax_smem[];
+    uint16_t* tile = reinterpret_cast<uint16_t*>(amax_smem);
+    uint32_t* ws = p.amax_ws;
+    const int64_t n_row_strips = p.R / TILE;
     const int t = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.y * TILE, c0 = (int64_t)blockIdx.x * TILE;
     uint32_t m = 0;
+    if (p.pre != PRE_NONE) {
+        load_tile(p, r0, c0, tile, false);
+        __syncthreads();
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         int q = t + i * THREADS;
         int rr = q >> 4, cc = (q & 15) * 8;
-        uint4 d = *reinterpret_cast<const uint4*>(x + (r0 + rr) * ld + c0 + cc);
+        uint4 d = p.pre != PRE_NONE ? *reinterpret_cast<const uint4*>(&tile[rr * LDS + cc])
+                                    : *reinterpret_cast<const uint4*>(p.x + (r0 + rr) * p.ld + c0 + cc);
         uint32_t w[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
@@ -401,7 +479,8 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
     if (nv) {
         size_t ws_bytes = (size_t)(1 + p.R / TILE + p.C / TILE) * 4;
         if (cudaMemsetAsync(p.amax_ws, 0, ws_bytes, stream) != cudaSuccess) return FP4_ERR_CUDA;
-        nv_amax_kernel<<<grid, THREADS, 0, stream>>>(p.x, p.R, p.ld, p.amax_ws, p.R / TILE);
+        const size_t amax_smem = p.pre != PRE_NONE ? sizeof(uint16_t) * TILE * LDS : 0;
+        nv_amax_kernel<<<grid, THREADS, amax_smem, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return FP4_ERR_CUDA;
         static bool attr_nv = false;
         if (!attr_nv) {

@@ -178,6 +178,78 @@ FP4_API int fp4_linear_dgrad(const fp4_tensor* dy_row, const fp4_tensor* w_col, 
 FP4_API int fp4_linear_wgrad(const fp4_tensor* dy_col, const fp4_tensor* x_col, float* dw, float beta,
                      fp4_stream_t stream);
 
+/* Fused gated-FFN forward producer (Sec. 3.2).  One contraction over the
+ * paired projections,
+ *   a1 = X W1^T, a3 = X W3^T     (x_row: Q_r(X) [T][d]; w13_row: Q_r of the
+ *                                 stacked [W1; W3] [2f][d], rows [0,f) = W1),
+ * whose epilogue writes the retained BF16 values a1, a3 (device bf16
+ * [T][f], the exact values autograd needs) and h = bf16(fl32(silu(a1)) * a3):
+ *   MXFP4  h is emitted directly as Q_r(h) [T][f] (W2 Fprop input) and
+ *          Q_c(h) [f][T] (W2 Wgrad input) into h_row / h_col;
+ *   NVFP4  the outer factors of h need its full-strip maximum, so h is
+ *          written to h_tap (required) and quantized with fp4_quantize;
+ *          h_row / h_col must be NULL.
+ * h_tap (device bf16 [T][f]) is optional for MXFP4.  T % 128 == 0,
+ * f % 128 == 0, d % 256 == 0.  Errors: FP4_ERR_INVALID_ARG,
+ * FP4_ERR_UNSUPPORTED_SHAPE, FP4_ERR_ROUTE_MISMATCH, FP4_ERR_CUDA. */
+FP4_API int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f, void* a1, void* a3,
+                           fp4_tensor* h_row, fp4_tensor* h_col, void* h_tap, fp4_stream_t stream);
+
+/* Fused gated-FFN backward producer (Sec. 3.2).  The W2 data-gradient
+ * contraction dh = dY2 W2 (dy2_row: Q_r(dY2) [T][d]; w2_col: Q_c(W2) [f][d])
+ * with, in its epilogue, dh = bf16(acc) and the SiLU derivative from the
+ * retained a1, a3 (device bf16 [T][f]):
+ *   da1 = bf16(dh * a3 * s * (1 + a1 * (1 - s))),  da3 = bf16(dh * a1 * s),
+ *   s = 1 / (1 + exp(-a1)),
+ * laid out as one logical tensor da13 = [da1 | da3] of [T][2f]:
+ *   MXFP4  emitted as Q_r(da13) [T][2f] with stochastic rounding (Philox
+ *          under sr_seed / sr_offset, element index t * 2f + c; the W1/W3
+ *          Dgrad operand, K = 2f) and Q_c(da13) [2f][T] (the W1/W3 Wgrad
+ *          operand) into da13_row / da13_col;
+ *   NVFP4  written to da13_tap (required) for fp4_quantize; views NULL.
+ * dh_tap (bf16 [T][f]) and da13_tap (bf16 [T][2f]) are optional for MXFP4. */
+FP4_API int fp4_swiglu_bwd(const fp4_tensor* dy2_row, const fp4_tensor* w2_col, int64_t f, const void* a1,
+                           const void* a3, uint64_t sr_seed, uint64_t sr_offset, fp4_tensor* da13_row,
+                           fp4_tensor* da13_col, void* dh_tap, void* da13_tap, fp4_stream_t stream);
+
+/* Residual + RMSNorm producer, forward (Sec. 3.2: the residual-RMSNorm
+ * boundary retains the exact residual and its row statistics while producing
+ * the next quantized representations).  For each row of r, b (device bf16,
+ * rows x cols, leading dimension ld; b may be NULL for b = 0) and gain g
+ * (device bf16 [cols]):
+ *   r_out = r' = bf16(r + b)                  device bf16 [rows][cols], retained
+ *   rstd  = fl32(1 / sqrt(mean(r'^2) + eps))   device binary32 [rows], retained
+ *   y     = bf16(fl32(fl32(r' * rstd) * g))   quantized into y_row / y_col
+ * exactly as fp4_quantize would quantize y under (route, views, flags 0);
+ * y_tap (device bf16 [rows][cols], optional) receives y itself.
+ * workspace: fp4_quantize_workspace_bytes(route, rows, cols, ...) bytes.
+ * Errors as fp4_quantize. */
+FP4_API int fp4_residual_rmsnorm_fwd(int route, unsigned views, const void* r, const void* b, const void* g,
+                                     int64_t rows, int64_t cols, int64_t ld, float eps, void* r_out, float* rstd,
+                                     fp4_tensor* y_row, fp4_tensor* y_col, void* y_tap, void* workspace,
+                                     size_t workspace_bytes, fp4_stream_t stream);
+
+/* Residual + RMSNorm producer, backward.  dy (device bf16 [rows][cols]) is the
+ * gradient of y, r_prime / rstd the state retained by the forward, g the gain
+ * and dres (device bf16 [rows][cols], may be NULL) the gradient arriving on the
+ * residual stream.  Computes, per row, mean_g = mean(fl32(dy * g) * fl32(r' * rstd))
+ * and
+ *   dr = bf16(fl32(fl32(rstd * fl32(fl32(dy * g) - fl32(fl32(r' * rstd) * mean_g))) + dres))
+ * written to dr (device bf16 [rows][cols], the residual gradient), and
+ * quantizes dr into dr_row (with FP4_FLAG_SR_ROW semantics under sr_seed /
+ * sr_offset when `sr` is non-zero) and dr_col: the gradient producer of the
+ * preceding linear.
+ * workspace: fp4_rmsnorm_bwd_workspace_bytes() bytes. */
+FP4_API int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, const void* r_prime,
+                                     const float* rstd, const void* g, const void* dres, int64_t rows, int64_t cols,
+                                     uint64_t sr_seed, uint64_t sr_offset, void* dr, fp4_tensor* dr_row,
+                                     fp4_tensor* dr_col, void* workspace, size_t workspace_bytes,
+                                     fp4_stream_t stream);
+
+/* Workspace of fp4_residual_rmsnorm_bwd: rows * 4 bytes of row statistics
+ * plus the quantizer's workspace, rounded up to 256 bytes.  Host only. */
+FP4_API int fp4_rmsnorm_bwd_workspace_bytes(int route, int64_t rows, int64_t cols, size_t* bytes);
+
 /* Read the sticky device status word (first device-side error since the last
  * reset, FP4_OK if none) into *code.  Synchronises `stream`. */
 FP4_API int fp4_status(fp4_stream_t stream, int* code);

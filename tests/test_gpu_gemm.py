@@ -120,3 +120,23 @@ def test_route_mismatch_is_rejected():
     with pytest.raises(F.Fp4Error) as e:
         F.fp4_linear_fprop(xr, wr)
     assert e.value.code == F.FP4_ERR_ROUTE_MISMATCH
+
+
+@pytest.mark.parametrize("M,N,K,route", [(384, 384, 512, "mx"), (2048, 4096, 512, "mx"), (2048, 2048, 768, "nv_local"),
+                                         (640, 768, 256, "nv_global")])
+def test_persistent_tiles_unpaired_and_narrow(M, N, K, route):
+    """Shapes that make CTAs loop over several tiles, use unpaired M blocks
+    (no cluster) and the 128-wide N tile; checked on sampled entries."""
+    bs, fmt = (32, 0) if route == "mx" else (16, 1)
+    a = normal_bf16((M, K), 1.0, M + N, 1)
+    b = normal_bf16((N, K), 0.05, M + N, 2)
+    ar, _ = F.fp4_quantize(to_dev(a), route, F.FP4_VIEW_ROW)
+    br, _ = F.fp4_quantize(to_dev(b), route, F.FP4_VIEW_ROW)
+    c = F.fp4_linear_fprop(ar, br).cpu().numpy()
+    ha, hb = host_view(ar, bs, fmt), host_view(br, bs, fmt)
+    rng = np.random.default_rng(0)
+    ms = np.concatenate([rng.integers(0, M, 4000), np.repeat(np.arange(M - 128, M), 8)])
+    ns = np.concatenate([rng.integers(0, N, 4000), np.tile(rng.integers(0, N, 8), 128)])
+    ref, absref = oracle.gemm_sampled(ha, hb, ms, ns)
+    assert_close(c[ms, ns], ref, absref, f"{route} {M}x{N}x{K}")
+    assert F.fp4_status() == F.FP4_OK
