@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 using namespace fp4;
@@ -382,6 +384,60 @@ int fp4_linear_dgrad(const fp4_tensor* dy_row, const fp4_tensor* w_col, void* dx
 
 int fp4_linear_wgrad(const fp4_tensor* dy_col, const fp4_tensor* x_col, float* dw, float beta, fp4_stream_t stream) {
     return linear(dy_col, x_col, dw, FP4_OUT_F32, beta, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free quantizer entry point.
+//
+// Some callers cannot call cudaMalloc at the moment they quantize: a runtime
+// that owns all device memory through its own pool and forbids raw
+// allocations, a serving process that reserves every byte at start-up, or code
+// on a latency-critical path where cudaMalloc's implicit device
+// synchronisation is not acceptable.  fp4_quantize_noalloc serves them by
+// taking the NVFP4 amax scratch from a fixed array in static device memory
+// instead of a caller-provided workspace.
+//
+// The array is FP4_NOALLOC_SCRATCH_BYTES (16 KiB) per GPU that loads this
+// library, held until the process exits, shared by every call on that GPU.
+// Each call clears the slots it uses before its amax pass, but the array keeps
+// the last call's contents, so calls whose kernels overlap on the GPU (other
+// streams, or concurrent host threads) race on it and must be serialised by
+// the caller.
+#define FP4_NOALLOC_SCRATCH_BYTES 16384
+static __device__ __align__(256) uint32_t g_noalloc_scratch[FP4_NOALLOC_SCRATCH_BYTES / 4];
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// with cudaGetSymbolAddress once per device (with that device current) and
+// cached.
+static void* noalloc_scratch(void) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
+int fp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld, int route, unsigned views,
+                         unsigned flags, uint64_t sr_seed, uint64_t sr_offset, const int8_t* hadamard_signs,
+                         fp4_tensor* row_out, fp4_tensor* col_out, fp4_stream_t stream) {
+    size_t need = 0;
+    int rc = fp4_quantize_workspace_bytes(route, rows, cols, views, flags, &need);
+    if (rc != FP4_OK) return rc;
+    if (need > FP4_NOALLOC_SCRATCH_BYTES) return FP4_ERR_WORKSPACE;
+    void* ws = nullptr;
+    if (need > 0 && rows > 0 && cols > 0) {
+        ws = noalloc_scratch();
+        if (!ws) return FP4_ERR_CUDA;
+    }
+    return fp4_quantize(x, rows, cols, ld, route, views, flags, sr_seed, sr_offset, hadamard_signs, row_out, col_out,
+                        ws, need, stream);
 }
 
 int fp4_status(fp4_stream_t stream, int* code) {

@@ -160,6 +160,26 @@ FP4_API int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, 
                  fp4_tensor* row_out, fp4_tensor* col_out, void* workspace, size_t workspace_bytes,
                  fp4_stream_t stream);
 
+/* fp4_quantize without a workspace argument, for callers that cannot
+ * allocate device memory when they quantize (a runtime whose pool owns all
+ * device memory, a server that reserves everything at start-up, a path that
+ * cannot afford cudaMalloc's implicit synchronisation).  The paper has no
+ * counterpart to this call; it is a deployment convenience.
+ *  - Same arguments, results and errors as fp4_quantize, except that the NVFP4
+ *    amax scratch comes from a 16 KiB array in static device memory that
+ *    every GPU loading this library holds until exit.  A shape needing more
+ *    (1 + rows/128 + cols/128 > 4096 slots) returns FP4_ERR_WORKSPACE.
+ *  - The call allocates nothing and frees nothing.
+ *  - All calls on a GPU share the array and each clears it before use: calls
+ *    whose kernels overlap on the GPU race, so the caller must order them
+ *    (one stream, or explicit synchronisation).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture begins. */
+FP4_API int fp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld, int route, unsigned views,
+                                 unsigned flags, uint64_t sr_seed, uint64_t sr_offset, const int8_t* hadamard_signs,
+                                 fp4_tensor* row_out, fp4_tensor* col_out, fp4_stream_t stream);
+
 /* The three contractions of Sec. 2.3 (Eqs. 4-6).  Each computes
  *   C[m][n] = alpha(m, n) * sum_k A_hat[m][k] * B_hat[n][k] + beta * C[m][n]
  * over K-major operands with FP32 tensor-core accumulation, where A_hat/B_hat
