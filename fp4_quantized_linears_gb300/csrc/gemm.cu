@@ -32,8 +32,11 @@
 //               every CTA of the cluster by a multicast tcgen05.commit;
 //   warps 2-9   epilogue: drain the accumulator from TMEM into registers
 //               (each warp one lane quarter x one column half), release it so
-//               the next tile's MMAs start, then finish and store the tile
-//               while the tensor core runs the next one.
+//               the next tile's MMAs start, then finish the tile while the
+//               tensor core runs the next one: plain outputs go through a
+//               128B-swizzled 32 x 128-byte shared buffer per warp and a TMA
+//               tensor store (or TMA reduce-add for beta = 1), so every
+//               global write is a full-line bulk transfer.
 // Every mbarrier wait is bounded: a wait that runs out sets the sticky status
 // word to FP4_ERR_TIMEOUT, the roles drain what they issued and the CTA
 // returns, releasing its tensor memory.
@@ -133,6 +136,27 @@ FP4_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
                  : "memory");
 }
 
+// TMA tensor store / reduce-add of a shared-memory box (bulk-group completion).
+FP4_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)map),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+FP4_DEV void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     (uint64_t)map),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+FP4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most N committed bulk groups may still be reading their shared source
+template <int N>
+FP4_DEV void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+FP4_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+FP4_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 FP4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 FP4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -188,7 +212,6 @@ FP4_DEV void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_
 FP4_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
-
 // 32 lanes x 32 columns of 32-bit accumulator; the wait is part of the same
 // asm statement, so no use of the registers can be scheduled before it.
 FP4_DEV void tmem_ld32(uint32_t taddr, uint32_t* r) {
@@ -300,7 +323,7 @@ struct KParams {
 
 template <bool NV, int BN, int EPI>
 struct Cfg {
-    static constexpr int STAGES = EPI == EPI_STORE ? 4 : (BN == 256 ? 3 : 4);
+    static constexpr int STAGES = BN != 256 ? 4 : 3;
     static constexpr int SF_CHUNKS = NV ? 4 : 2;  // 512-byte atoms per 128 rows per stage
     static constexpr int A_BYTES = BM * BK_BYTES;
     static constexpr int B_BYTES = BN * BK_BYTES;
@@ -310,7 +333,10 @@ struct Cfg {
     static constexpr int SF_COLS_A = SF_CHUNKS * 4;
     static constexpr int SF_COLS_B = SF_CHUNKS * (BN / 32);
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    static constexpr int STAGING = EPI == EPI_STORE ? 0 : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
+    // STORE: per epilogue warp one or two 32-row x 128-byte buffers for TMA stores
+    static constexpr int OUT_BUFS = STAGES * STAGE_BYTES + EPI_WARPS * 2 * 4096 + 1280 <= 232448 ? 2 : 1;
+    static constexpr int STAGING =
+        EPI == EPI_STORE ? EPI_WARPS * OUT_BUFS * 4096 : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
     static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + 256 /*barriers*/;
     static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -319,7 +345,8 @@ struct Cfg {
 
 template <bool NV, int BN, int EPI, int CM>
 __global__ void __launch_bounds__(THREADS, 1)
-    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, KParams p) {
+    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, KParams p) {
     using C = Cfg<NV, BN, EPI>;
     constexpr int STAGES = C::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -467,6 +494,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t sfa_col = sf_base + stage * C::SF_COLS;
                 const uint32_t sfb_col = sfa_col + C::SF_COLS_A;
+                // scale atoms -> TMEM (replicated into the four lane quarters)
 #pragma unroll
                 for (int c = 0; c < C::SF_CHUNKS; ++c) {
                     tc_cp_sf(sfa_col + 4 * c, smem_desc(smem_u32(stage_sfa(stage) + c * 512), 0, 128, LAYOUT_NONE));
@@ -479,9 +507,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t a_base = smem_u32(stage_a(stage)), b_base = smem_u32(stage_b(stage));
 #pragma unroll
                 for (int kk = 0; kk < BK / 64; ++kk) {
-                    uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
-                    uint64_t bd = smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
-                    uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    const uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
+                    const uint64_t bd = smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     if (NV) {
                         mma_nvf4(tmem, ad, bd, make_idesc(BN, false, 0, 0), sfa_col + 4 * kk, sfb_col + kk * (BN / 32),
                                  acc);
@@ -545,37 +573,84 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(acc_empty);
                 float sa = 1.0f;
                 if (NV) sa = __fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]);
+                const bool tma_out = p.beta == 0.0f || p.beta == 1.0f;
+                if (tma_out) {
+                    // rows [32q, 32q+32) of the tile through this warp's two
+                    // 128B-swizzled 32 x 128-byte buffers and TMA stores
+                    uint8_t* wbuf = staging + (warp - 2) * C::OUT_BUFS * 4096;
+                    const bool f32 = p.out_dtype == FP4_OUT_F32;
+                    constexpr int NB = NC;  // boxes per thread: fp32 32 cols, bf16 64 cols
+                    const int nbox = f32 ? NB : NB / 2;
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const int64_t n = n0 + half * (BN / 2) + 32 * c;
-                    float alpha = 1.0f;
-                    if (NV) alpha = __fmul_rn(sa, __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n >> 7)]));
-                    const uint32_t* rc = r + 32 * c;
-                    if (p.out_dtype == FP4_OUT_F32) {
-                        float* dst = reinterpret_cast<float*>(p.c) + m * p.N + n;
+                    for (int bi = 0; bi < NB; ++bi) {
+                        if (bi >= nbox) break;
+                        uint8_t* buf = wbuf + (C::OUT_BUFS == 2 ? (bi & 1) * 4096 : 0);
+                        // the store previously issued from this buffer must have read it
+                        if (lane == 0) {
+                            if (C::OUT_BUFS == 2)
+                                bulk_wait_read<1>();
+                            else
+                                bulk_wait_read<0>();
+                        }
+                        __syncwarp();
+                        const int cols = f32 ? 32 : 64;
+                        const int64_t n = n0 + half * (BN / 2) + cols * bi;
+                        float alpha = 1.0f;
+                        if (NV) alpha = __fmul_rn(sa, __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n >> 7)]));
+                        uint32_t w[32];
+                        if (f32) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            float4 v = make_float4(__uint_as_float(rc[i]) * alpha, __uint_as_float(rc[i + 1]) * alpha,
-                                                   __uint_as_float(rc[i + 2]) * alpha,
-                                                   __uint_as_float(rc[i + 3]) * alpha);
-                            if (p.beta != 0.0f) {
-                                float4 o = *reinterpret_cast<const float4*>(dst + i);
+                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(r[32 * bi + i]) * alpha);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                w[i] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[64 * bi + 2 * i]) * alpha) |
+                                       ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[64 * bi + 2 * i + 1]) * alpha) << 16);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<uint4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (p.beta == 0.0f)
+                                tma_store_2d(&tmC, buf, (int)n, (int)(m0 + q * 32));
+                            else
+                                tma_reduce_add_2d(&tmC, buf, (int)n, (int)(m0 + q * 32));
+                            bulk_commit();
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const int64_t n = n0 + half * (BN / 2) + 32 * c;
+                        float alpha = 1.0f;
+                        if (NV) alpha = __fmul_rn(sa, __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n >> 7)]));
+                        const uint32_t* rc = r + 32 * c;
+                        if (p.out_dtype == FP4_OUT_F32) {
+                            float* dst = reinterpret_cast<float*>(p.c) + m * p.N + n;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                float4 v = make_float4(__uint_as_float(rc[i]) * alpha,
+                                                       __uint_as_float(rc[i + 1]) * alpha,
+                                                       __uint_as_float(rc[i + 2]) * alpha,
+                                                       __uint_as_float(rc[i + 3]) * alpha);
+                                const float4 o = *reinterpret_cast<const float4*>(dst + i);
                                 v.x += p.beta * o.x;
                                 v.y += p.beta * o.y;
                                 v.z += p.beta * o.z;
                                 v.w += p.beta * o.w;
+                                *reinterpret_cast<float4*>(dst + i) = v;
                             }
-                            *reinterpret_cast<float4*>(dst + i) = v;
-                        }
-                    } else {
-                        uint16_t* dst = reinterpret_cast<uint16_t*>(p.c) + m * p.N + n;
-                        float v[32];
+                        } else {
+                            uint16_t* dst = reinterpret_cast<uint16_t*>(p.c) + m * p.N + n;
+                            float v[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            v[i] = __uint_as_float(rc[i]) * alpha;
-                            if (p.beta != 0.0f) v[i] += p.beta * bf16_to_f32(dst[i]);
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = __uint_as_float(rc[i]) * alpha + p.beta * bf16_to_f32(dst[i]);
+                            store_bf16x32(dst, v);
                         }
-                        store_bf16x32(dst, v);
                     }
                 }
             } else if constexpr (EPI == EPI_SWIGLU_FWD) {
@@ -743,6 +818,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             acc_phase ^= 1;
         }
     }
+    if (EPI == EPI_STORE && warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores done with shared memory
     tc_fence_before();
     __syncthreads();
     if (CM > 1) cluster_sync();  // no peer still multicasts into this CTA
@@ -780,6 +856,20 @@ bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K) {
     return r == CUDA_SUCCESS;
 }
 
+// Row-major output [M][N] (fp32 or bf16), box 128 bytes x 32 rows, 128B swizzle.
+bool make_out_map(CUtensorMap* map, void* c, int64_t M, int64_t N, int out_dtype) {
+    const bool f32 = out_dtype == FP4_OUT_F32;
+    const int es = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(N * es)};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32u};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cached[64] = {};
     int dev = 0;
@@ -796,8 +886,11 @@ int sm_count() {
 template <bool NV, int BN, int EPI, int CM>
 int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream_t stream) {
     using C = Cfg<NV, BN, EPI>;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     if (!make_map(&ta, g.a_codes, g.M, g.K) || !make_map(&tb, g.b_codes, g.b_rows, g.K)) return FP4_ERR_CUDA;
+    memset(&tc, 0, sizeof tc);
+    if (EPI == EPI_STORE && (g.beta == 0.0f || g.beta == 1.0f) && !make_out_map(&tc, g.c, g.M, g.N, g.out_dtype))
+        return FP4_ERR_CUDA;
     auto kern = fp4_gemm_kernel<NV, BN, EPI, CM>;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -829,7 +922,7 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
     }
     const int64_t clusters = n_units < max_clusters ? n_units : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * CM));
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, kp) != cudaSuccess) return FP4_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp) != cudaSuccess) return FP4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 

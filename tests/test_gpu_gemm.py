@@ -110,7 +110,13 @@ def test_bf16_output_and_beta_accumulate():
     assert torch.equal(yb, y32.to(torch.bfloat16))
     acc = y32.clone()
     F.fp4_linear_fprop(xr, wr, y=acc, beta=1.0)
-    assert torch.allclose(acc, 2 * y32, rtol=1e-6, atol=0)
+    assert torch.equal(acc, 2 * y32)
+    acc = y32.clone()
+    F.fp4_linear_fprop(xr, wr, y=acc, beta=0.5)
+    assert torch.allclose(acc, 1.5 * y32, rtol=1e-6, atol=0)
+    accb = yb.clone()
+    F.fp4_linear_fprop(xr, wr, y=accb, out_dtype=F.FP4_OUT_BF16, beta=1.0)
+    assert torch.allclose(accb.float(), 2 * yb.float(), rtol=2 ** -7, atol=0)
 
 
 def test_route_mismatch_is_rejected():
