@@ -289,6 +289,10 @@ def run_ours(args):
             tf = gemm_flops / (v * 1e-3) / 1e12
             kernels[n] = {"ms": round(v, 4), "TFLOP/s": round(tf, 1), "fp4_frac": round(tf / fp4_peak, 4)}
 
+    # free the main workload's buffers before the other legs
+    del X, W, DY, Y, DX, DW, xr, xc, wr, wc, dr, dc, dX2, dW2, dDY2
+    torch.cuda.empty_cache()
+    legs = {} if args.no_legs else run_legs(args, peaks)
     cpu = cpu_baseline_sample(seconds_target=args.cpu_seconds) if args.cpu_seconds > 0 else None
     line = {
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -307,11 +311,145 @@ def run_ours(args):
         "gpu_launches": args.steps * 6,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "legs": legs,
         "input_gen_s": round(gen_s, 1),
     }
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+# ------------------------------------------------------------ other legs ----
+def _timed(fn, steps: int, warmup: int) -> float:
+    """Mean device milliseconds of fn() over `steps` calls after `warmup`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_legs(args, peaks, only=None) -> dict:
+    """The other workloads of the boundary, each one pass per step:
+    NVFP4 (global and CTA-local) on attention-projection shapes, the fused
+    SwiGLU FFN forward + backward, and the 32-block 27/5 depth-hybrid stack."""
+    import torch
+    import fp4_quantized_linears_gb300 as F
+    from fp4_quantized_linears_gb300.stack import BlockShape, FP4LinearStack, linear_flops_per_token
+    from synthetic import config_tensors
+    fp4_peak = peaks["bf16"] * FP4_NOMINAL_OVER_BF16
+    out = {}
+
+    def dev(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+
+    def frac(tf):
+        return round(tf / fp4_peak, 4)
+
+    # NVFP4 attention projections: X 8192x4096, W 4096x4096 and 6144x4096
+    if only not in (None, "nvfp4"):
+        t3 = None
+    else:
+        t3 = config_tensors("c3_nv_attn", scale_T=args.tokens)
+    X3 = dev(t3["x"]) if t3 is not None else None
+    for route in (("nv_global", "nv_local") if t3 is not None else ()):
+        for wname, dyname in (("w", "dy"), ("w_qkv", "dy_qkv")):
+            Wt, DYt = dev(t3[wname]), dev(t3[dyname])
+            n_out, n_in = Wt.shape
+            T3 = X3.shape[0]
+            ws = torch.empty(max(F.fp4_quantize_workspace_bytes(route, T3, n_out), F.fp4_quantize_workspace_bytes(route, n_out, n_in), 16), dtype=torch.uint8, device="cuda")
+            xr, xc = F.alloc_view(route, T3, n_in), F.alloc_view(route, n_in, T3)
+            wr, wc = F.alloc_view(route, n_out, n_in, F.FP4_FLAG_WEIGHT_2D), F.alloc_view(route, n_in, n_out, F.FP4_FLAG_WEIGHT_2D)
+            dr, dc = F.alloc_view(route, T3, n_out), F.alloc_view(route, n_out, T3)
+            Y = torch.empty((T3, n_out), device="cuda")
+            DXo = torch.empty((T3, n_in), device="cuda")
+            DWo = torch.empty((n_out, n_in), device="cuda")
+
+            def step3():
+                F.fp4_quantize(X3, route, 3, 0, row_out=xr, col_out=xc, workspace=ws)
+                F.fp4_quantize(Wt, route, 3, F.FP4_FLAG_WEIGHT_2D, row_out=wr, col_out=wc, workspace=ws)
+                F.fp4_quantize(DYt, route, 3, F.FP4_FLAG_SR_ROW, sr_seed=2, row_out=dr, col_out=dc, workspace=ws)
+                F.fp4_linear_fprop(xr, wr, Y)
+                F.fp4_linear_dgrad(dr, wc, DXo)
+                F.fp4_linear_wgrad(dc, xc, DWo)
+
+            ms = _timed(step3, 5, 3)
+            gemm_ms = _timed(lambda: (F.fp4_linear_fprop(xr, wr, Y), F.fp4_linear_dgrad(dr, wc, DXo),
+                                      F.fp4_linear_wgrad(dc, xc, DWo)), 5, 2)
+            fl = 3 * 2.0 * T3 * n_in * n_out
+            out[f"nvfp4_{route.split('_')[1]}_{n_out}x{n_in}"] = {
+                "ms_per_step": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
+                "gemm_TFLOP/s": round(fl / gemm_ms / 1e9, 1), "gemm_fp4_frac": frac(fl / gemm_ms / 1e9)}
+            del Wt, DYt, xr, xc, wr, wc, dr, dc, Y, DXo, DWo, ws
+    del X3, t3
+    torch.cuda.empty_cache()
+
+    if only not in (None, "swiglu"):
+        return out
+    # fused SwiGLU FFN, MXFP4, T 16384, d 4096, f 14336
+    t4 = config_tensors("c4_swiglu", scale_T=args.tokens)
+    X4, W13, W2, DY2 = dev(t4["x"]), dev(t4["w13"]), dev(t4["w2"]), dev(t4["dy2"])
+    del t4
+    T4, d4 = X4.shape
+    f4 = W2.shape[1]
+    xr, xc = F.alloc_view("mx", T4, d4), F.alloc_view("mx", d4, T4)
+    w13r, w13c = F.alloc_view("mx", 2 * f4, d4), F.alloc_view("mx", d4, 2 * f4)
+    w2r, w2c = F.alloc_view("mx", d4, f4), F.alloc_view("mx", f4, d4)
+    dyr, dyc = F.alloc_view("mx", T4, d4), F.alloc_view("mx", d4, T4)
+    a1 = torch.empty((T4, f4), dtype=torch.bfloat16, device="cuda")
+    a3 = torch.empty_like(a1)
+    hr, hc = F.alloc_view("mx", T4, f4), F.alloc_view("mx", f4, T4)
+    dar, dac = F.alloc_view("mx", T4, 2 * f4), F.alloc_view("mx", 2 * f4, T4)
+    Y2 = torch.empty((T4, d4), dtype=torch.bfloat16, device="cuda")
+    DX4 = torch.empty((T4, d4), dtype=torch.bfloat16, device="cuda")
+    DW13 = torch.empty((2 * f4, d4), device="cuda")
+    DW2 = torch.empty((d4, f4), device="cuda")
+
+    def step4():
+        F.fp4_quantize(X4, "mx", 3, 0, row_out=xr, col_out=xc)
+        F.fp4_quantize(W13, "mx", 3, F.FP4_FLAG_WEIGHT_2D, row_out=w13r, col_out=w13c)
+        F.fp4_quantize(W2, "mx", 3, F.FP4_FLAG_WEIGHT_2D, row_out=w2r, col_out=w2c)
+        F.fp4_swiglu_fwd(xr, w13r, f4, a1=a1, a3=a3, h_row=hr, h_col=hc)
+        F.fp4_linear_fprop(hr, w2r, Y2, F.FP4_OUT_BF16)
+        F.fp4_quantize(DY2, "mx", 3, F.FP4_FLAG_SR_ROW, sr_seed=3, row_out=dyr, col_out=dyc)
+        F.fp4_swiglu_bwd(dyr, w2c, f4, a1, a3, sr_seed=3, sr_offset=1, da13_row=dar, da13_col=dac)
+        F.fp4_linear_dgrad(dar, w13c, DX4, F.FP4_OUT_BF16)
+        F.fp4_linear_wgrad(dac, xc, DW13)
+        F.fp4_linear_wgrad(dyc, hc, DW2)
+
+    ms = _timed(step4, 3, 2)
+    fl4 = 18.0 * T4 * d4 * f4
+    ms_fwd = _timed(lambda: F.fp4_swiglu_fwd(xr, w13r, f4, a1=a1, a3=a3, h_row=hr, h_col=hc), 3, 1)
+    ms_bwd = _timed(lambda: F.fp4_swiglu_bwd(dyr, w2c, f4, a1, a3, sr_seed=3, sr_offset=1, da13_row=dar,
+                                             da13_col=dac), 3, 1)
+    out["swiglu_ffn_mxfp4_T16384"] = {
+        "ms_per_step": round(ms, 3), "TFLOP/s": round(fl4 / ms / 1e9, 1), "tokens_per_s": round(T4 / ms * 1e3, 1),
+        "fused_fwd_ms": round(ms_fwd, 4), "fused_fwd_TFLOP/s": round(4.0 * T4 * d4 * f4 / ms_fwd / 1e9, 1),
+        "fused_bwd_ms": round(ms_bwd, 4), "fused_bwd_TFLOP/s": round(2.0 * T4 * d4 * f4 / ms_bwd / 1e9, 1)}
+    del X4, W13, W2, DY2, xr, xc, w13r, w13c, w2r, w2c, dyr, dyc, a1, a3, hr, hc, dar, dac, Y2, DX4, DW13, DW2
+    torch.cuda.empty_cache()
+
+    # 32-block depth hybrid (blocks 1-27 CTA-local NVFP4, 28-32 MXFP4), T 8192
+    if not args.no_stack and only is None:
+        sh = BlockShape()
+        st = FP4LinearStack(32, 27, sh, seed=5)
+        g = torch.Generator(device="cuda").manual_seed(5)
+        x5 = torch.randn((sh.T, sh.d), generator=g, device="cuda").to(torch.bfloat16)
+        dy5 = (torch.randn((sh.T, sh.d), generator=g, device="cuda") * 1e-4).to(torch.bfloat16)
+        ms = _timed(lambda: st.step(x5, dy5, sr_seed=5), 2, 1)
+        fl5 = linear_flops_per_token(sh) * 32 * sh.T
+        out["stack32_hybrid_27nv_5mx_T8192"] = {
+            "ms_per_step": round(ms, 2), "tokens_per_s": round(sh.T / ms * 1e3, 1),
+            "linear_TFLOP/s": round(fl5 / ms / 1e9, 1), "linear_tflop_per_step": round(fl5 / 1e12, 2)}
+        del st, x5, dy5
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------ CPU oracle ----
@@ -404,6 +542,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-legs", action="store_true", help="only the main workload")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 32-block stack leg")
+    ap.add_argument("--only", choices=["nvfp4", "swiglu"], default=None,
+                    help="run just one of the other legs (sized by --tokens) and print its numbers")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count (default 8192); smaller values make a profiling-sized case")
     args = ap.parse_args()
@@ -414,6 +556,10 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps({"only": args.only, "legs": run_legs(args, load_peaks(), args.only)}), flush=True)
     else:
         run_ours(args)
 

@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int i = 0; i < 32; ++i) {
                         x1[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r1[32 * c + i]) * alpha));
                         x3[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r3[32 * c + i]) * alpha));
-                        const float s = __fdiv_rn(x1[i], __fadd_rn(1.0f, expf(-x1[i])));
+                        const float s = x1[i] * __frcp_rn(1.0f + __expf(-x1[i]));
                         h[i] = bf16_to_f32(f32_to_bf16_rn(__fmul_rn(s, x3[i])));
                     }
                     store_bf16x32(p.a1 + m * p.f + n, x1);
@@ -760,7 +760,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int j = 0; j < 8; ++j) {
                                 const float x = (j & 1) ? bf16_hi(w1[j >> 1]) : bf16_lo(w1[j >> 1]);
                                 const float y = (j & 1) ? bf16_hi(w3[j >> 1]) : bf16_lo(w3[j >> 1]);
-                                const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
+                                const float sg = __frcp_rn(1.0f + __expf(-x));
                                 const float g = dh[i + j];
                                 const float dsilu = sg * (1.0f + x * (1.0f - sg));
                                 d1[i + j] = bf16_to_f32(f32_to_bf16_rn(g * y * dsilu));
