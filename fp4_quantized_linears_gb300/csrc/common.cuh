@@ -34,8 +34,8 @@ FP4_DEV uint16_t f32_to_bf16_rn(float f) {
 // --------------------------------------------------------------- E2M1 RN ---
 // Two binary32 values -> one byte of two E2M1 codes, `lo` in the low nibble,
 // round to nearest even with saturation at 6 (the hardware conversion).  The
-// sign of every input is copied into its code, so a negative value that
-// rounds to zero keeps its sign bit.
+// conversion keeps the sign of a value that rounds to zero (code 8 for -0.1),
+// which the exhaustive quantizer parity tests check against the oracle.
 FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
     uint32_t r;
     asm("{\n\t.reg .b8 t;\n\t"
@@ -43,8 +43,7 @@ FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
         "cvt.u32.u8 %0, t;\n\t}"
         : "=r"(r)
         : "f"(hi), "f"(lo));
-    uint32_t s = ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
-    return r | s;
+    return r;
 }
 
 // --------------------------------------------------------------- E2M1 SR ---
@@ -120,13 +119,14 @@ FP4_DEV uint32_t nv_block_scale(float block_amax, float senc, float& mult) {
 }
 
 // -------------------------------------------------------------- Philox ----
-// Philox4x32-10: ten rounds of the 4x32 S-box with key increments.
+// Philox4x32-10: ten rounds of the 4x32 S-box with key increments.  Each
+// round's two 32x32 -> 64-bit products are single widening multiplies.
 FP4_DEV uint4 philox4x32_10(uint4 c, uint2 k) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.x, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k.y, (uint32_t)p0);
         k.x += 0x9E3779B9u;
         k.y += 0xBB67AE85u;
     }

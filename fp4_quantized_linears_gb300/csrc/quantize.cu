@@ -45,8 +45,15 @@ struct SmemQ {
     int tile_e[16];                  // 2D32: per 32x32 tile exponent
     float tile_m[64];                // 2D16: per 16x16 tile multiplier
     uint32_t tile_d[64];             // 2D16: per 16x16 tile E4M3 byte
+    uint32_t seg_amax[TILE * 8];     // 2D: |max| bits of each 16-value row piece
     uint32_t red[THREADS / 32];
 };
+
+// Column-view code staging is segment-major with the stored row XOR-ed by the
+// segment index, so that both the encoding threads (consecutive stored rows)
+// and the write-out threads (four segments of a row) hit at most two lanes
+// per bank.
+FP4_DEV int col_stage_off(int c, int j) { return j * 2048 + ((c ^ j) << 4); }
 
 // Byte offset of local block j (0..nb-1) of local row r in staged atoms.
 FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
@@ -138,6 +145,21 @@ FP4_DEV void hadamard32_nosign(float* v) {
 // applying the pre-op; with write_tap the pre-op results are also stored.
 FP4_DEV void load_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* tile, bool write_tap) {
     const int t = threadIdx.x;
+    if (p.pre == PRE_NONE) {
+        // all eight 16-byte loads of this thread in flight before any store
+        uint4 d[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = t + i * THREADS;
+            d[i] = *reinterpret_cast<const uint4*>(p.x + (r0 + (q >> 4)) * p.ld + c0 + (q & 15) * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = t + i * THREADS;
+            *reinterpret_cast<uint4*>(&tile[(q >> 4) * LDS + (q & 15) * 8]) = d[i];
+        }
+        return;
+    }
 #pragma unroll 2
     for (int i = 0; i < 8; ++i) {
         int q = t + i * THREADS;
@@ -213,7 +235,7 @@ FP4_DEV void unpack_lane(const uint32_t* w, int h, float* v) {
 }
 
 template <bool NV>
-__global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
+__global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
     const int t = threadIdx.x;
@@ -246,43 +268,55 @@ __global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
     }
     __syncthreads();
 
-    // 2. shared 2D weight scales
+    // 2. shared 2D weight scales: the maxima of the 16-value pieces of every
+    //    row (16-byte shared loads), then one reduction per tile
     if (w2d) {
-        const int warp = t >> 5, lane = t & 31;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
+            const uint16_t* src = &s.tile[r * LDS + j * 32];
+            uint32_t w[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
+                w[4 * q] = d.x; w[4 * q + 1] = d.y; w[4 * q + 2] = d.z; w[4 * q + 3] = d.w;
+            }
+            const uint32_t a0 = amax_words<8>(w), a1 = amax_words<8>(w + 8);
+            s.seg_amax[r * 8 + 2 * j] = max(lane_lo_f32bits(a0), lane_hi_f32bits(a0));
+            s.seg_amax[r * 8 + 2 * j + 1] = max(lane_lo_f32bits(a1), lane_hi_f32bits(a1));
+        }
+        __syncthreads();
         if (!NV) {
-            // 16 tiles of 32x32: warp w handles tiles 2w, 2w+1; lane = row
-            for (int k = 0; k < 2; ++k) {
-                int tile = warp * 2 + k, tr = tile >> 2, tc = tile & 3;
-                uint32_t m = 0;
-                const uint16_t* row = &s.tile[(tr * 32 + lane) * LDS + tc * 32];
+            // 16 tiles of 32x32: 16 threads per tile, two rows each
+            const int tile = t >> 4, part = t & 15, tr = tile >> 2, tc = tile & 3;
+            uint32_t m = 0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) m = max(m, ((uint32_t)row[j] << 16) & 0x7FFFFFFFu);
+            for (int i = 0; i < 2; ++i) {
+                const int r = tr * 32 + part * 2 + i;
+                m = max(m, max(s.seg_amax[r * 8 + 2 * tc], s.seg_amax[r * 8 + 2 * tc + 1]));
+            }
 #pragma unroll
-                for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                if (lane == 0) {
-                    check_finite(m);
-                    int e = e8m0_exponent_up(m);
-                    // adaptive rule: finer exponent when a_T * 2^-e < fl32(5.22)
-                    if (__fmul_rn(__uint_as_float(m), exp2_neg(e)) < 5.22f && e > -127) e -= 1;
-                    s.tile_e[tile] = e;
-                }
+            for (int o = 8; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (part == 0) {
+                check_finite(m);
+                int e = e8m0_exponent_up(m);
+                // adaptive rule: finer exponent when a_T * 2^-e < fl32(5.22)
+                if (__fmul_rn(__uint_as_float(m), exp2_neg(e)) < 5.22f && e > -127) e -= 1;
+                s.tile_e[tile] = e;
             }
         } else {
-            // 64 tiles of 16x16: warp w handles tiles 8w .. 8w+7, two at a time
-            for (int k = 0; k < 4; ++k) {
-                int tile = warp * 8 + k * 2 + (lane >> 4), tr = tile >> 3, tc = tile & 7;
-                const uint16_t* row = &s.tile[(tr * 16 + (lane & 15)) * LDS + tc * 16];
-                uint32_t m = 0;
+            // 64 tiles of 16x16: 4 threads per tile, four rows each
+            const int tile = t >> 2, part = t & 3, tr = tile >> 3, tc = tile & 7;
+            uint32_t m = 0;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) m = max(m, ((uint32_t)row[j] << 16) & 0x7FFFFFFFu);
-#pragma unroll
-                for (int o = 8; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                if ((lane & 15) == 0) {
-                    check_finite(m);
-                    float mm;
-                    s.tile_d[tile] = nv_block_scale(__uint_as_float(m), senc_row, mm);
-                    s.tile_m[tile] = mm;
-                }
+            for (int i = 0; i < 4; ++i) m = max(m, s.seg_amax[(tr * 16 + part * 4 + i) * 8 + tc]);
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            if (part == 0) {
+                check_finite(m);
+                float mm;
+                s.tile_d[tile] = nv_block_scale(__uint_as_float(m), senc_row, mm);
+                s.tile_m[tile] = mm;
             }
         }
         __syncthreads();
@@ -391,7 +425,7 @@ __global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
             } else {
                 segment_scale<NV>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1);
             }
-            *reinterpret_cast<uint4*>(&s.col_codes[c * 64 + j * 16]) = pack_rn32(v, m0, m1);
+            *reinterpret_cast<uint4*>(&s.col_codes[col_stage_off(c, j)]) = pack_rn32(v, m0, m1);
         }
     }
     __syncthreads();
@@ -417,7 +451,7 @@ __global__ void __launch_bounds__(THREADS) quantize_tile_kernel(QuantParams p) {
         for (int k = 0; k < 2; ++k) {
             int q = t + k * THREADS, cc = q >> 2, part = q & 3;
             *reinterpret_cast<uint4*>(p.col_codes + (c0 + cc) * (p.R >> 1) + (r0 >> 1) + part * 16) =
-                *reinterpret_cast<const uint4*>(&s.col_codes[cc * 64 + part * 16]);
+                *reinterpret_cast<const uint4*>(&s.col_codes[col_stage_off(cc, part)]);
         }
         const int nat = NV ? 2 : 1;
         if (t < nat * 32) {
@@ -485,6 +519,7 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
         static bool attr_nv = false;
         if (!attr_nv) {
             cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             attr_nv = true;
         }
         quantize_tile_kernel<true><<<grid, THREADS, smem, stream>>>(p);
@@ -492,6 +527,7 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
         static bool attr_mx = false;
         if (!attr_mx) {
             cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             attr_mx = true;
         }
         quantize_tile_kernel<false><<<grid, THREADS, smem, stream>>>(p);
