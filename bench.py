@@ -49,6 +49,37 @@ def gemm_bytes_min() -> float:
     return 0.0
 
 
+KERNEL_SOURCES = {
+    "gemm": ("gemm.cu", "common.cuh", "internal.h"),
+    "quant": ("quantize.cu", "common.cuh", "internal.h"),
+}
+
+
+def _sources_digest(kind: str) -> str:
+    import hashlib
+    m = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "fp4_quantized_linears_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel` from the ncu summaries
+    under profiles/, or None when none was taken of the current sources."""
+    import glob
+    want = _sources_digest("quant" if kernel.startswith("quant") else "gemm")
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for line in f:
+                if not line.startswith("traffic-record "):
+                    continue
+                kv = dict(tok.split("=", 1) for tok in line.split()[1:])
+                if kv.get("kernel") == kernel and kv.get("sources") == want:
+                    return int(kv["bytes"])
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -272,13 +303,13 @@ def run_ours(args):
     if dom in ("fprop", "dgrad", "wgrad"):
         ach = gemm_flops / (per_kernel[dom] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp4_peak, 1),
-                "unit": "TFLOP/s", "frac": round(ach / fp4_peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(ach / fp4_peak, 4), "traffic": profiled_traffic(dom),
                 "peak_note": f"{peaks['src']} bf16 burst {peaks['bf16']} x nominal fp4/bf16 ratio 6"}
     else:
         b = pb[dom.split("_")[1]]
         ach = b / (per_kernel[dom] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm"], 4), "traffic": None, "peak_note": f"{peaks['src']} hbm_gbs"}
+                "frac": round(ach / peaks["hbm"], 4), "traffic": profiled_traffic(dom), "peak_note": f"{peaks['src']} hbm_gbs"}
     kernels = {}
     for n, v in per_kernel.items():
         if n.startswith("quant"):
