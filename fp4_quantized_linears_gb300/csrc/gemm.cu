@@ -58,8 +58,10 @@ __device__ unsigned int g_status_gemm;
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 256;  // FP4 elements per stage (128 bytes per row)
+constexpr int BK = 256;  // FP4 elements per stage: 128-byte rows, 128-byte swizzle
 constexpr int BK_BYTES = BK / 2;
+constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
+constexpr int MAX_STAGES = 8;
 constexpr int THREADS = 320;
 constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 512;
@@ -179,6 +181,10 @@ FP4_DEV uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t l
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 constexpr uint32_t LAYOUT_SW128 = 2;
+constexpr uint32_t LAYOUT_SW64 = 4;
+// operand tiles: K-major rows of BK_BYTES, swizzled across 8-row groups
+constexpr uint32_t AB_LAYOUT = BK_BYTES == 128 ? LAYOUT_SW128 : LAYOUT_SW64;
+constexpr uint32_t AB_SBO = 8 * BK_BYTES;
 constexpr uint32_t LAYOUT_NONE = 0;
 
 // Instruction descriptor of the block-scaled kinds: E2M1 A and B (format 1),
@@ -321,26 +327,40 @@ struct KParams {
     uint64_t seed, offset;
 };
 
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+// The ring is as deep as shared memory and the TMEM scale-factor region
+// allow (up to MAX_STAGES): the operand loads of the next stages are what
+// hides the L2/HBM latency.  (Halving BK to deepen the ring measured slower:
+// 64-byte rows cost more than the extra depth gains.)
 template <bool NV, int BN, int EPI>
 struct Cfg {
-    static constexpr int STAGES = BN != 256 ? 4 : 3;
-    static constexpr int SF_CHUNKS = NV ? 4 : 2;  // 512-byte atoms per 128 rows per stage
+    static constexpr int SF_CHUNKS = NV ? BK / 64 : BK / 128;  // 512-byte atoms per 128 rows per stage
     static constexpr int A_BYTES = BM * BK_BYTES;
     static constexpr int B_BYTES = BN * BK_BYTES;
     static constexpr int SFA_BYTES = SF_CHUNKS * 512;
     static constexpr int SFB_BYTES = (BN / 128) * SF_CHUNKS * 512;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int TX_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // bytes landing per stage
+    static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;           // ring slot, 1 KiB aligned
     static constexpr int SF_COLS_A = SF_CHUNKS * 4;
     static constexpr int SF_COLS_B = SF_CHUNKS * (BN / 32);
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    // STORE: per epilogue warp one or two 32-row x 128-byte buffers for TMA stores
-    static constexpr int OUT_BUFS = STAGES * STAGE_BYTES + EPI_WARPS * 2 * 4096 + 1280 <= 232448 ? 2 : 1;
+    static constexpr int RESERVED = 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int fit(int staging) {
+        return cmin(MAX_STAGES, cmin((SMEM_LIMIT - RESERVED - staging) / STAGE_BYTES, (TMEM_COLS - SF_COL0) / SF_COLS));
+    }
+    // STORE: per epilogue warp two 32-row x 128-byte buffers for TMA stores,
+    // or one where two would cost the ring a stage
+    static constexpr int OUT_BUFS =
+        EPI != EPI_STORE ? 0 : (fit(EPI_WARPS * 2 * 4096) >= fit(EPI_WARPS * 4096) ? 2 : 1);
     static constexpr int STAGING =
         EPI == EPI_STORE ? EPI_WARPS * OUT_BUFS * 4096 : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int STAGES = fit(STAGING);
+    static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + RESERVED;
+    static_assert(STAGES >= 3, "pipeline depth");
     static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
-    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
+    static_assert(2 * MAX_STAGES * 8 + 64 <= 256, "barrier area");
 };
 
 template <bool NV, int BN, int EPI, int CM>
@@ -433,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+                mbar_expect_tx(&full[stage], C::TX_BYTES);
                 tma_load_2d(stage_a(stage), &tmA, kb * BK_BYTES, (int)m0, &full[stage]);
                 if (CM > 1) {
                     // this CTA's 128-row share of B, delivered to the whole cluster
@@ -507,8 +527,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t a_base = smem_u32(stage_a(stage)), b_base = smem_u32(stage_b(stage));
 #pragma unroll
                 for (int kk = 0; kk < BK / 64; ++kk) {
-                    const uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024, LAYOUT_SW128);
-                    const uint64_t bd = smem_desc(b_base + kk * 32, 16, 1024, LAYOUT_SW128);
+                    // each MMA's 64 FP4 values start 32 bytes further into the rows
+                    const uint64_t ad = smem_desc(a_base + kk * 32, 16, AB_SBO, AB_LAYOUT);
+                    const uint64_t bd = smem_desc(b_base + kk * 32, 16, AB_SBO, AB_LAYOUT);
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     if (NV) {
                         mma_nvf4(tmem, ad, bd, make_idesc(BN, false, 0, 0), sfa_col + 4 * kk, sfb_col + kk * (BN / 32),
@@ -851,7 +872,8 @@ bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K) {
     cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, 128u};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, BK_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
