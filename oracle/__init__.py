@@ -92,9 +92,10 @@ def _declare(L):
         "orc_hadamard32_f32": (None, [_f32p, _i8p]),
         "orc_hadamard32_rows": (None, [_f32p, _i64, _i64, _i8p]),
         "orc_sylvester_h32": (None, [_i8p]),
-        "orc_mx_quantize_rows": (None, [_f32p, _i64, _i64, ctypes.c_int, _u64, _u64, _u8p, _u8p]),
+        "orc_mx_quantize_rows": (None, [_f32p, _i64, _i64, ctypes.c_int, _u64, _u64, _u64, _i64, _u8p, _u8p]),
         "orc_mx_quantize_weight2d": (None, [_f32p, _i64, _i64, _u8p, _u8p]),
-        "orc_nv_quantize_rows": (None, [_f32p, _i64, _i64, _f32p, ctypes.c_int, _u64, _u64, _u8p, _u8p]),
+        "orc_nv_quantize_rows": (None, [_f32p, _i64, _i64, _f32p, ctypes.c_int, _u64, _u64, _u64, _i64, _u8p,
+                                         _u8p]),
         "orc_nv_quantize_weight2d": (None, [_f32p, _i64, _i64, ctypes.c_float, _u8p, _u8p]),
         "orc_amax_f32": (ctypes.c_float, [_f32p, _i64]),
         "orc_bf16_to_f32": (None, [_u16p, _i64, _f32p]),
@@ -214,21 +215,23 @@ def amax_f32(x: np.ndarray) -> float:
 # tensor quantizers
 # ---------------------------------------------------------------------------
 
-def _mx_rows(xf: np.ndarray, sr: bool, seed: int, offset: int):
+def _mx_rows(xf: np.ndarray, sr: bool, seed: int, offset: int, index0: int = 0, ld: int | None = None):
     R, C = xf.shape
     codes = np.empty((R, C), np.uint8)
     scales = np.empty((R, C // 32), np.uint8)
-    lib().orc_mx_quantize_rows(_p(xf, _f32p), R, C, int(sr), seed, offset, _p(codes, _u8p), _p(scales, _u8p))
+    lib().orc_mx_quantize_rows(_p(xf, _f32p), R, C, int(sr), seed, offset, index0, C if ld is None else ld,
+                               _p(codes, _u8p), _p(scales, _u8p))
     return codes, scales
 
 
-def _nv_rows(xf: np.ndarray, senc_row: np.ndarray, sr: bool, seed: int, offset: int):
+def _nv_rows(xf: np.ndarray, senc_row: np.ndarray, sr: bool, seed: int, offset: int, index0: int = 0,
+             ld: int | None = None):
     R, C = xf.shape
     codes = np.empty((R, C), np.uint8)
     scales = np.empty((R, C // 16), np.uint8)
     s = np.ascontiguousarray(senc_row, dtype=np.float32)
-    lib().orc_nv_quantize_rows(_p(xf, _f32p), R, C, _p(s, _f32p), int(sr), seed, offset,
-                               _p(codes, _u8p), _p(scales, _u8p))
+    lib().orc_nv_quantize_rows(_p(xf, _f32p), R, C, _p(s, _f32p), int(sr), seed, offset, index0,
+                               C if ld is None else ld, _p(codes, _u8p), _p(scales, _u8p))
     return codes, scales
 
 
@@ -243,8 +246,14 @@ def _strip_senc(xf: np.ndarray) -> np.ndarray:
     return out
 
 
+def _sr_index(origin, cols, C):
+    ld = C if cols is None else int(cols)
+    return int(origin[0]) * ld + int(origin[1]), ld
+
+
 def quantize(x_bits: np.ndarray, route: str, view: str, *, sr: bool = False, seed: int = 0,
-             offset: int = 0, hadamard: bool = False, signs=None, weight2d: bool = False) -> dict:
+             offset: int = 0, hadamard: bool = False, signs=None, weight2d: bool = False,
+             sr_origin: tuple[int, int] = (0, 0), sr_cols: int | None = None) -> dict:
     """Quantize a bf16 tensor (uint16 bits, R x C) into one view.
 
     route    'mx' | 'nv_global' | 'nv_local'
@@ -252,6 +261,11 @@ def quantize(x_bits: np.ndarray, route: str, view: str, *, sr: bool = False, see
     sr       stochastic rounding; only allowed on the row view (Sec. 2.5)
     hadamard fixed-sign H32 before quantization; only on the MX column view
     weight2d 2D32 (MX) or 2D16 (NV) shared weight encoding (Sec. 2.4)
+    sr_origin, sr_cols
+             when x is a block of a larger tensor: the (row, column) of its
+             first element there and the larger tensor's row length, so that
+             stochastic rounding draws the counters of the whole tensor's
+             logical indices (defaults: x is the whole tensor)
 
     Returns dict(codes=uint8[rows, cols] 4-bit codes of the stored view,
                  scales=uint8[rows, cols // bs], senc=float32[rows] or None,
@@ -293,13 +307,13 @@ def quantize(x_bits: np.ndarray, route: str, view: str, *, sr: bool = False, see
         v = v.copy()
         lib().orc_hadamard32_rows(_p(v, _f32p), v.shape[0], v.shape[1], _p(s, _i8p))
     if route == "mx":
-        codes, scales = _mx_rows(v, sr, seed, offset)
+        codes, scales = _mx_rows(v, sr, seed, offset, *_sr_index(sr_origin, sr_cols, C))
         return dict(codes=codes, scales=scales, senc=None, fmt=0, bs=32)
     if route == "nv_global":
         senc_row = np.full(v.shape[0], nv_senc(amax_f32(xf)), np.float32)
     else:
         senc_row = _strip_senc(v)
-    codes, scales = _nv_rows(v, senc_row, sr, seed, offset)
+    codes, scales = _nv_rows(v, senc_row, sr, seed, offset, *_sr_index(sr_origin, sr_cols, C))
     return dict(codes=codes, scales=scales, senc=senc_row, fmt=1, bs=16)
 
 

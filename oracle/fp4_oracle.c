@@ -307,9 +307,12 @@ void orc_sylvester_h32(int8_t* h)
 /* MXFP4, 32-value blocks with upward E8M0 scales (Sec. 2.2.1).  x holds
  * binary32 values (bf16 inputs widened exactly, or H32 outputs).  With
  * sr != 0 the values are rounded stochastically (Sec. 2.5) using the
- * row-major logical index r * C + c. */
+ * row-major logical index of the element in the whole tensor,
+ * index0 + r * ld + c: x may be a block of rows and columns of a larger
+ * tensor whose element (0, 0) has logical index index0 and whose rows are
+ * ld long (index0 = 0, ld = C for a whole tensor). */
 void orc_mx_quantize_rows(const float* x, int64_t R, int64_t C, int sr, uint64_t seed,
-                          uint64_t offset, uint8_t* codes, uint8_t* scales)
+                          uint64_t offset, uint64_t index0, int64_t ld, uint8_t* codes, uint8_t* scales)
 {
     for (int64_t r = 0; r < R; ++r)
         for (int64_t b = 0; b < C / 32; ++b) {
@@ -322,7 +325,8 @@ void orc_mx_quantize_rows(const float* x, int64_t R, int64_t C, int sr, uint64_t
             for (int j = 0; j < 32; ++j) {
                 float v = (float)((double)blk[j] * ldexp(1.0, -e)); /* fl32 */
                 int64_t i = r * C + b * 32 + j;
-                codes[i] = sr ? orc_e2m1_sr((double)v, orc_sr_uniform16(seed, offset, (uint64_t)i))
+                uint64_t li = index0 + (uint64_t)(r * ld + b * 32 + j);
+                codes[i] = sr ? orc_e2m1_sr((double)v, orc_sr_uniform16(seed, offset, li))
                               : orc_e2m1_rn((double)v);
             }
         }
@@ -358,9 +362,10 @@ void orc_mx_quantize_weight2d(const float* x, int64_t R, int64_t C, uint8_t* cod
 /* NVFP4, 16-value blocks with E4M3 scales under a binary32 outer factor
  * (Sec. 2.2.2).  senc_row[r] is the S_enc that applies to row r: one value
  * for the whole tensor (global NVFP4) or the factor of the row's 128-row
- * strip (CTA-local NVFP4).  sr as for MXFP4. */
+ * strip (CTA-local NVFP4).  sr, index0 and ld as for MXFP4. */
 void orc_nv_quantize_rows(const float* x, int64_t R, int64_t C, const float* senc_row, int sr,
-                          uint64_t seed, uint64_t offset, uint8_t* codes, uint8_t* scales)
+                          uint64_t seed, uint64_t offset, uint64_t index0, int64_t ld, uint8_t* codes,
+                          uint8_t* scales)
 {
     for (int64_t r = 0; r < R; ++r)
         for (int64_t b = 0; b < C / 16; ++b) {
@@ -373,7 +378,8 @@ void orc_nv_quantize_rows(const float* x, int64_t R, int64_t C, const float* sen
             for (int j = 0; j < 16; ++j) {
                 float v = blk[j] * m; /* fl32 */
                 int64_t i = r * C + b * 16 + j;
-                codes[i] = sr ? orc_e2m1_sr((double)v, orc_sr_uniform16(seed, offset, (uint64_t)i))
+                uint64_t li = index0 + (uint64_t)(r * ld + b * 16 + j);
+                codes[i] = sr ? orc_e2m1_sr((double)v, orc_sr_uniform16(seed, offset, li))
                               : orc_e2m1_rn((double)v);
             }
         }

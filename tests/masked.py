@@ -1,0 +1,94 @@
+"""Comparison of FP4 views whose pre-quantization values are produced on the
+GPU by an FP32 computation that the oracle does not repeat bit for bit: the
+accumulation order of a contraction, the device exponential of SiLU, the
+order of a row reduction.
+
+The expected views always come from the oracle run on host inputs alone.
+The GPU's own BF16 values (the retained tensors or a debug tap) are used
+only to decide where the comparison can be exact: every scale block whose
+BF16 inputs are identical on both sides must match bit for bit, the blocks
+that differ must be few, and there the GPU codes must still be a valid
+encoding of the GPU's values (checked with the small decoder below, which
+is test code, not the oracle)."""
+import numpy as np
+
+from layout import expand_outer, unpack_codes, unswizzle_scales
+
+E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def bf16_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def e4m3_f64(b: np.ndarray) -> np.ndarray:
+    b = b.astype(np.int64)
+    e, m = (b >> 3) & 15, b & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+def host_view(v):
+    """Codes [rows, cols], scale bytes [rows, cols/bs] and the per-row outer
+    factor (or None) of a GPU view, unpacked on the host."""
+    import torch
+    import fp4_quantized_linears_gb300 as F
+    torch.cuda.synchronize()
+    bs = 32 if v.route == F.FP4_ROUTE_MXFP4 else 16
+    return dict(codes=unpack_codes(v.codes.cpu().numpy()),
+                scales=unswizzle_scales(v.scales.cpu().numpy(), v.rows, v.cols, bs),
+                senc=None if v.outer is None else expand_outer(v.outer.cpu().numpy(), v.outer_count, v.rows),
+                bs=bs, fmt=0 if bs == 32 else 1)
+
+
+def oriented(vals: np.ndarray, view: str) -> np.ndarray:
+    """The [R, C] tensor in the stored orientation of a view."""
+    return vals if view == "row" else np.ascontiguousarray(vals.T)
+
+
+def decode(h: dict) -> np.ndarray:
+    """Decoded values of a view, [rows, cols] in binary64."""
+    q = E2M1[h["codes"]]
+    rep = np.repeat(h["scales"], h["bs"], axis=1)
+    if h["fmt"] == 0:
+        return q * 2.0 ** (rep.astype(np.float64) - 127.0)
+    out = q * e4m3_f64(rep)
+    senc = h["senc"]
+    return out / np.asarray(senc, np.float64)[:, None]
+
+
+def _step(a: np.ndarray) -> np.ndarray:
+    """E2M1 grid spacing at magnitude a (in units of the block scale)."""
+    return np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+
+
+def assert_view_masked(got: dict, want: dict, gpu_vals: np.ndarray, same_vals: np.ndarray, what: str,
+                       max_bad_frac: float = 0.05):
+    """got/want: host views (GPU / oracle) of one orientation; gpu_vals and
+    same_vals: the GPU's BF16 inputs of that view and the element mask where
+    they equal the oracle's, both [rows, cols] in the view's orientation."""
+    bs = want["bs"]
+    rows, cols = want["codes"].shape
+    ok = same_vals.reshape(rows, cols // bs, bs).all(2)
+    if want["senc"] is not None:
+        # an outer factor covers a whole strip of stored rows: where it
+        # differs (its amax element differs), nothing in the strip is exact
+        same_outer = np.asarray(got["senc"]) == np.asarray(want["senc"])
+        ok &= same_outer[:, None]
+    bad_frac = 1.0 - ok.mean()
+    assert bad_frac <= max_bad_frac, f"{what}: {bad_frac:.2%} of blocks differ in their inputs"
+    okm = np.repeat(ok, bs, axis=1)
+    nc = int(np.sum((got["codes"] != want["codes"]) & okm))
+    ns = int(np.sum((got["scales"] != want["scales"]) & ok))
+    assert nc == 0 and ns == 0, f"{what}: {nc} code / {ns} scale mismatches in blocks with identical inputs"
+    if (~ok).any():
+        # validity where the inputs differ: the GPU encoding of the GPU values
+        # is within one grid step of them at the block's own scale
+        v = bf16_f64(gpu_vals)
+        dec = decode(got)
+        unit = decode(dict(got, codes=np.full_like(got["codes"], 2)))  # code 2 decodes to 1.0 x block scale
+        err = np.abs(dec - v)
+        bound = _step(np.minimum(np.abs(v) / np.maximum(unit, 1e-300), 6.0)) * unit * 1.0001
+        # an NVFP4 block whose E4M3 scale rounds to zero decodes to zero
+        bad = ~okm & ~(err <= bound) & (unit > 0)
+        assert not bad.any(), f"{what}: {int(bad.sum())} codes are not a valid encoding of the GPU values"
+    return bad_frac

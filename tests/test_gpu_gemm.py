@@ -2,9 +2,12 @@
 contraction of the dequantized operands (Format-Aware Fusion for Fast FP4
 Pretraining, Sec. 2.3 Eqs. 4-6).
 
-Tolerance (fixed by the build's contract): relative Frobenius error <= 1e-5
-and, per element, |err| <= 2^-18 * sum_k |a_k b_k|.  Operands with unit scales
-and integer-valued products are exact in FP32 and must match bit for bit."""
+The reference operands are the oracle's own quantization of the host inputs;
+the GPU's views are first required to equal them bit for bit, so the GPU
+contraction and the reference contract the same codes.  Tolerance: relative
+Frobenius error <= 1e-5 and, per element, |err| <= 2^-18 * sum_k |a_k b_k|.
+Operands with unit scales and integer-valued products are exact in FP32 and
+must match bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -41,6 +44,26 @@ def assert_close(got: np.ndarray, ref: np.ndarray, absref: np.ndarray, what: str
     assert (err <= PER_ELEM * absref + 1e-30).all(), f"{what}: max err / sum|ab| = {ratio:.3e} (> 2^-18)"
 
 
+def same_view(got: dict, want: dict, what: str):
+    assert np.array_equal(got["codes"], want["codes"]), f"{what}: codes differ from the oracle's"
+    assert np.array_equal(got["scales"], want["scales"]), f"{what}: scales differ from the oracle's"
+    if want["senc"] is not None:
+        assert np.array_equal(got["senc"], want["senc"]), f"{what}: outer factors differ from the oracle's"
+
+
+def oracle_views(x, w, dy, route, xflags=0, dyflags=0, signs=None, seed=0, offset=0):
+    """The six operand views as the oracle quantizes the host inputs."""
+    hx = bool(xflags & F.FP4_FLAG_HADAMARD_COL)
+    hd = bool(dyflags & F.FP4_FLAG_HADAMARD_COL)
+    sr = bool(dyflags & F.FP4_FLAG_SR_ROW)
+    return dict(xr=oracle.quantize(x, route, "row"),
+                xc=oracle.quantize(x, route, "col", hadamard=hx, signs=signs),
+                wr=oracle.quantize(w, route, "row", weight2d=True),
+                wc=oracle.quantize(w, route, "col", weight2d=True),
+                dr=oracle.quantize(dy, route, "row", sr=sr, seed=seed, offset=offset),
+                dc=oracle.quantize(dy, route, "col", hadamard=hd, signs=signs))
+
+
 def run_linear(x, w, dy, route, xflags=0, dyflags=0, signs=None, seed=0, offset=0):
     bs, fmt = (32, 0) if route == "mx" else (16, 1)
     xr, xc = F.fp4_quantize(to_dev(x), route, 3, xflags, hadamard_signs=signs)
@@ -50,8 +73,10 @@ def run_linear(x, w, dy, route, xflags=0, dyflags=0, signs=None, seed=0, offset=
     dx = F.fp4_linear_dgrad(dr, wc)
     dw = F.fp4_linear_wgrad(dc, xc)
     torch.cuda.synchronize()
-    hv = {k: host_view(v, bs, fmt) for k, v in dict(xr=xr, xc=xc, wr=wr, wc=wc, dr=dr, dc=dc).items()}
-    return y.cpu().numpy(), dx.cpu().numpy(), dw.cpu().numpy(), hv
+    ov = oracle_views(x, w, dy, route, xflags, dyflags, signs, seed, offset)
+    for k, v in dict(xr=xr, xc=xc, wr=wr, wc=wc, dr=dr, dc=dc).items():
+        same_view(host_view(v, bs, fmt), ov[k], f"{route} {k}")
+    return y.cpu().numpy(), dx.cpu().numpy(), dw.cpu().numpy(), ov
 
 
 @pytest.mark.parametrize("route", ["mx", "nv_global", "nv_local"])
@@ -139,7 +164,9 @@ def test_persistent_tiles_unpaired_and_narrow(M, N, K, route):
     ar, _ = F.fp4_quantize(to_dev(a), route, F.FP4_VIEW_ROW)
     br, _ = F.fp4_quantize(to_dev(b), route, F.FP4_VIEW_ROW)
     c = F.fp4_linear_fprop(ar, br).cpu().numpy()
-    ha, hb = host_view(ar, bs, fmt), host_view(br, bs, fmt)
+    ha, hb = oracle.quantize(a, route, "row"), oracle.quantize(b, route, "row")
+    same_view(host_view(ar, bs, fmt), ha, "A")
+    same_view(host_view(br, bs, fmt), hb, "B")
     rng = np.random.default_rng(0)
     ms = np.concatenate([rng.integers(0, M, 4000), np.repeat(np.arange(M - 128, M), 8)])
     ns = np.concatenate([rng.integers(0, N, 4000), np.tile(rng.integers(0, N, 8), 128)])

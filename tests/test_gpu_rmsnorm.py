@@ -1,15 +1,18 @@
 """GPU parity of the residual-RMSNorm producer (Format-Aware Fusion for Fast
-FP4 Pretraining, Sec. 3.2), in two levels: the retained BF16 state and the
-BF16 values it quantizes are checked against the oracle's model arithmetic,
-then the FP4 views are checked bit for bit against the oracle quantizing
-those same BF16 values."""
+FP4 Pretraining, Sec. 3.2) against the oracle run on the host inputs alone.
+The residual r' is exact; the FP32 row statistic may differ from the
+oracle's binary64 one by an ulp (the kernel sums in a tree), so y is exact on
+the rows whose statistic agrees and within one bf16 ulp elsewhere; the FP4
+views are bit for bit in every scale block whose BF16 inputs agree with the
+oracle's and a valid encoding of the kernel's values in the others."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import fp4_quantized_linears_gb300 as F
-from layout import expand_outer, unpack_codes, unswizzle_scales
+from masked import assert_view_masked, oriented
+from masked import host_view as mhost
 from synthetic import normal_bf16
 
 pytestmark = pytest.mark.gpu
@@ -29,16 +32,6 @@ def ordered(b):
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
-def assert_view(v, ref, what):
-    torch.cuda.synchronize()
-    codes = unpack_codes(v.codes.cpu().numpy())
-    scales = unswizzle_scales(v.scales.cpu().numpy(), v.rows, v.cols, ref["bs"])
-    assert np.array_equal(codes, ref["codes"]), f"{what}: {np.sum(codes != ref['codes'])} code mismatches"
-    assert np.array_equal(scales, ref["scales"]), f"{what}: scale mismatch"
-    if ref["senc"] is not None:
-        assert np.array_equal(expand_outer(v.outer.cpu().numpy(), v.outer_count, v.rows), ref["senc"]), what
-
-
 @pytest.mark.parametrize("route", ["mx", "nv_global", "nv_local"])
 def test_rmsnorm_forward(route):
     R, C = 256, 512
@@ -47,18 +40,22 @@ def test_rmsnorm_forward(route):
     g = normal_bf16((C,), 1.0, 21, 3)
     tap = torch.empty((R, C), dtype=torch.bfloat16, device="cuda")
     rp, rstd, yr, yc = F.fp4_residual_rmsnorm_fwd(to_dev(r), to_dev(b), to_dev(g), route, y_tap=tap)
-    o_rp, o_rstd, _ = oracle.residual_rmsnorm(r, b, g, 1e-5)
+    assert F.fp4_status() == F.FP4_OK
+    o_rp, o_rstd, o_y = oracle.residual_rmsnorm(r, b, g, 1e-5)
     assert np.array_equal(bits(rp), o_rp), "r' must be the exact bf16 residual"
     g_rstd = rstd.cpu().numpy()
     ulps = np.abs(g_rstd.view(np.int32) - o_rstd.view(np.int32))
     assert ulps.max() <= 2, f"rstd differs by {ulps.max()} ulp"
-    # y from the kernel's own row statistic is bit-exact
-    _, _, y_ref = oracle.residual_rmsnorm(r, b, g, 1e-5, rstd_in=g_rstd)
+    # rows whose FP32 statistic equals the oracle's give the oracle's y exactly
     y = bits(tap)
-    assert np.array_equal(y, y_ref)
-    assert_view(yr, oracle.quantize(y, route, "row"), f"{route} y row")
-    assert_view(yc, oracle.quantize(y, route, "col"), f"{route} y col")
-    assert F.fp4_status() == F.FP4_OK
+    same_row = g_rstd == o_rstd
+    assert np.array_equal(y[same_row], o_y[same_row])
+    d = np.abs(ordered(y) - ordered(o_y))
+    assert d.max() <= 1
+    same = y == o_y
+    assert_view_masked(mhost(yr), oracle.quantize(o_y, route, "row"), y, same, f"{route} y row")
+    assert_view_masked(mhost(yc), oracle.quantize(o_y, route, "col"), oriented(y, "col"), oriented(same, "col"),
+                       f"{route} y col")
 
 
 @pytest.mark.parametrize("route", ["mx", "nv_local"])
@@ -71,11 +68,14 @@ def test_rmsnorm_backward(route):
     rstd = (1.0 / np.sqrt((oracle.bf16_to_f32(rp).astype(np.float64) ** 2).mean(1) + 1e-5)).astype(np.float32)
     dr, drr, drc = F.fp4_residual_rmsnorm_bwd(to_dev(dy), to_dev(rp), torch.from_numpy(rstd).cuda(), to_dev(g),
                                               to_dev(dres), route, sr=True, sr_seed=9, sr_offset=4)
+    assert F.fp4_status() == F.FP4_OK
     got = bits(dr)
     want = oracle.rmsnorm_bwd(dy, rp, rstd, g, dres)
     d = np.abs(ordered(got) - ordered(want))
     assert d.max() <= 1, f"dr differs by up to {d.max()} bf16 ulp"
     assert (d > 0).mean() < 0.02
-    assert_view(drr, oracle.quantize(got, route, "row", sr=True, seed=9, offset=4), f"{route} dr row")
-    assert_view(drc, oracle.quantize(got, route, "col"), f"{route} dr col")
-    assert F.fp4_status() == F.FP4_OK
+    same = got == want
+    assert_view_masked(mhost(drr), oracle.quantize(want, route, "row", sr=True, seed=9, offset=4), got, same,
+                       f"{route} dr row")
+    assert_view_masked(mhost(drc), oracle.quantize(want, route, "col"), oriented(got, "col"), oriented(same, "col"),
+                       f"{route} dr col")

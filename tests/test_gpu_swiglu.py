@@ -1,17 +1,19 @@
 """GPU parity of the fused gated-FFN producers (Format-Aware Fusion for Fast
-FP4 Pretraining, Sec. 3.2).  Two levels: the retained BF16 values (a1, a3,
-dh) against the oracle's binary64 contraction rounded to bf16 (<= 1 ulp, the
-FP32 accumulation can move a tie), the gate values (h, da1, da3) against the
-oracle's model arithmetic on the kernel's own retained values (<= 1 ulp:
-the device exp differs from the binary64 one), and the FP4 views bit for bit
-against the oracle quantizing the very BF16 values the kernel quantized."""
+FP4 Pretraining, Sec. 3.2), against the oracle's chain computed from the host
+inputs alone: the retained BF16 values (a1, a3, dh) within one bf16 ulp of
+the oracle's binary64 contraction rounded to bf16 (the FP32 accumulation can
+move a tie); the gate values (h, da1, da3) within one ulp of the oracle's
+where their inputs agree (the device exp differs from the binary64 one); the
+FP4 views bit for bit in every scale block whose BF16 inputs agree, and a
+valid encoding of the kernel's values in the few blocks that do not."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import fp4_quantized_linears_gb300 as F
-from layout import expand_outer, unpack_codes, unswizzle_scales
+from masked import assert_view_masked, oriented
+from masked import host_view as mhost
 from synthetic import normal_bf16
 
 pytestmark = pytest.mark.gpu
@@ -33,21 +35,6 @@ def ordered(b):
 
 def ulp(a, b):
     return np.abs(ordered(a) - ordered(b))
-
-
-def host_view(v, route):
-    torch.cuda.synchronize()
-    bs, fmt = (32, 0) if route == "mx" else (16, 1)
-    return dict(codes=unpack_codes(v.codes.cpu().numpy()),
-                scales=unswizzle_scales(v.scales.cpu().numpy(), v.rows, v.cols, bs),
-                senc=None if v.outer is None else expand_outer(v.outer.cpu().numpy(), v.outer_count, v.rows),
-                fmt=fmt, bs=bs)
-
-
-def assert_view(v, ref, what):
-    h = host_view(v, "mx" if ref["fmt"] == 0 else "nv")
-    assert np.array_equal(h["codes"], ref["codes"]), f"{what}: {np.sum(h['codes'] != ref['codes'])} code mismatches"
-    assert np.array_equal(h["scales"], ref["scales"]), f"{what}: scale mismatch"
 
 
 def check_bf16_gemm(got_bits, ref_f64, absref, what, max_frac=0.02):
@@ -74,17 +61,27 @@ def test_swiglu_forward(route, T):
     tap = torch.empty((T, f), dtype=torch.bfloat16, device="cuda")
     a1, a3, hr, hc = F.fp4_swiglu_fwd(xr, wr, f, h_tap=tap)
     assert F.fp4_status() == F.FP4_OK
-    qx, qw = host_view(xr, route), host_view(wr, route)
+    # the oracle's chain from the host inputs alone
+    qx = oracle.quantize(x, route, "row")
+    qw = oracle.quantize(w13, route, "row", weight2d=True)
     qw1 = {k: (v[:f] if isinstance(v, np.ndarray) else v) for k, v in qw.items()}
     qw3 = {k: (v[f:] if isinstance(v, np.ndarray) else v) for k, v in qw.items()}
-    check_bf16_gemm(bits(a1), oracle.gemm(qx, qw1), oracle.gemm_abs(qx, qw1), "a1")
-    check_bf16_gemm(bits(a3), oracle.gemm(qx, qw3), oracle.gemm_abs(qx, qw3), "a3")
-    h = bits(tap)
-    d_h = ulp(h, oracle.swiglu_h(bits(a1), bits(a3)))
+    c1, c3 = oracle.gemm(qx, qw1), oracle.gemm(qx, qw3)
+    o_a1, o_a3 = oracle.round_bf16(c1), oracle.round_bf16(c3)
+    o_h = oracle.swiglu_h(o_a1, o_a3)
+    g_a1, g_a3, g_h = bits(a1), bits(a3), bits(tap)
+    check_bf16_gemm(g_a1, c1, oracle.gemm_abs(qx, qw1), "a1")
+    check_bf16_gemm(g_a3, c3, oracle.gemm_abs(qx, qw3), "a3")
+    # where the contraction rounded alike, the gate value is the oracle's up
+    # to the device exponential (<= 1 bf16 ulp, rarely)
+    same_in = (g_a1 == o_a1) & (g_a3 == o_a3)
+    d_h = ulp(g_h, o_h)[same_in]
     assert d_h.max() <= 1 and (d_h > 0).mean() < 0.01
+    same_h = g_h == o_h
     if route == "mx":
-        assert_view(hr, oracle.quantize(h, "mx", "row"), "Q_r(h)")
-        assert_view(hc, oracle.quantize(h, "mx", "col"), "Q_c(h)")
+        assert_view_masked(mhost(hr), oracle.quantize(o_h, "mx", "row"), g_h, same_h, "Q_r(h)")
+        assert_view_masked(mhost(hc), oracle.quantize(o_h, "mx", "col"), oriented(g_h, "col"),
+                           oriented(same_h, "col"), "Q_c(h)")
     else:
         assert hr is None and hc is None
 
@@ -103,17 +100,24 @@ def test_swiglu_backward(route):
     rr, cc = F.fp4_swiglu_bwd(dr, wc, f, to_dev(a1), to_dev(a3), sr_seed=77, sr_offset=5, dh_tap=dh_tap,
                               da13_tap=da_tap)
     assert F.fp4_status() == F.FP4_OK
-    dh = bits(dh_tap)
-    hd, hw = host_view(dr, route), host_view(wc, route)
-    check_bf16_gemm(dh, oracle.gemm(hd, hw), oracle.gemm_abs(hd, hw), "dh")
-    da = bits(da_tap)
-    o1, o3 = oracle.swiglu_bwd(dh, a1, a3)
-    for got, want, name in ((da[:, :f], o1, "da1"), (da[:, f:], o3, "da3")):
-        dd = ulp(np.ascontiguousarray(got), want)
-        assert dd.max() <= 1 and (dd > 0).mean() < 0.01, name
+    # the oracle's chain from the host inputs alone
+    qd = oracle.quantize(dy2, route, "row", sr=True, seed=3, offset=1)
+    qw = oracle.quantize(w2, route, "col", weight2d=True)
+    c = oracle.gemm(qd, qw)
+    o_dh = oracle.round_bf16(c)
+    o1, o3 = oracle.swiglu_bwd(o_dh, a1, a3)
+    o_da = np.concatenate([o1, o3], axis=1)
+    g_dh, g_da = bits(dh_tap), bits(da_tap)
+    check_bf16_gemm(g_dh, c, oracle.gemm_abs(qd, qw), "dh")
+    same_dh = np.concatenate([g_dh == o_dh] * 2, axis=1)
+    dd = ulp(g_da, o_da)[same_dh]
+    assert dd.max() <= 1 and (dd > 0).mean() < 0.01, "da13"
+    same_da = g_da == o_da
     if route == "mx":
-        assert_view(rr, oracle.quantize(da, "mx", "row", sr=True, seed=77, offset=5), "Q_r(da13)")
-        assert_view(cc, oracle.quantize(da, "mx", "col"), "Q_c(da13)")
+        assert_view_masked(mhost(rr), oracle.quantize(o_da, "mx", "row", sr=True, seed=77, offset=5), g_da,
+                           same_da, "Q_r(da13)")
+        assert_view_masked(mhost(cc), oracle.quantize(o_da, "mx", "col"), oriented(g_da, "col"),
+                           oriented(same_da, "col"), "Q_c(da13)")
     else:
         assert rr is None and cc is None
 

@@ -135,3 +135,25 @@ def test_hadamard_col_view_preserves_dot_before_quantization():
     got = oracle.gemm(qd, qx)
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel < 0.2
+
+
+def test_sr_of_a_block_uses_the_whole_tensors_indices():
+    """Stochastic rounding draws its counter from the element's logical index
+    in the whole tensor (Sec. 2.5): a block quantized with its origin in the
+    larger tensor reproduces that block of the whole-tensor result, and the
+    same block quantized as a tensor of its own does not."""
+    x = normal_bf16((256, 512), 1.0, 61, 1)
+    r0, c0 = 128, 256
+    blk = np.ascontiguousarray(x[r0:r0 + 128, c0:c0 + 128])
+    whole = oracle.quantize(x, "mx", "row", sr=True, seed=5, offset=2)
+    part = oracle.quantize(blk, "mx", "row", sr=True, seed=5, offset=2, sr_origin=(r0, c0), sr_cols=512)
+    assert np.array_equal(part["codes"], whole["codes"][r0:r0 + 128, c0:c0 + 128])
+    alone = oracle.quantize(blk, "mx", "row", sr=True, seed=5, offset=2)
+    assert not np.array_equal(alone["codes"], part["codes"])
+    # CTA-local NVFP4: a 128-row strip carries its own factor, so a strip
+    # quantized with its origin equals the whole tensor's rows
+    whole = oracle.quantize(x, "nv_local", "row", sr=True, seed=5, offset=2)
+    strip = oracle.quantize(np.ascontiguousarray(x[r0:r0 + 128]), "nv_local", "row", sr=True, seed=5, offset=2,
+                            sr_origin=(r0, 0), sr_cols=512)
+    assert np.array_equal(strip["codes"], whole["codes"][r0:r0 + 128])
+    assert np.array_equal(strip["scales"], whole["scales"][r0:r0 + 128])
