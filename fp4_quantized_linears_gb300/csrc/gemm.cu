@@ -138,6 +138,26 @@ FP4_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
                  : "memory");
 }
 
+// ---- CTA pair (cta_group::2) ----
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+FP4_DEV uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Tensor load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (here: the pair leader's).
+FP4_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+FP4_DEV void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // TMA tensor store / reduce-add of a shared-memory box (bulk-group completion).
 FP4_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)map),
@@ -162,16 +182,30 @@ FP4_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;"
 FP4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 FP4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+template <int G = 1>
 FP4_DEV void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+    if (G == 2)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                     : "memory");
 }
+// arrive on the barrier at the same offset in every CTA of `mask`
+template <int G = 1>
 FP4_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
+    if (G == 2)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                smem_u32(bar)),
+            "h"(mask)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                smem_u32(bar)),
+            "h"(mask)
+            : "memory");
 }
 
 // shared-memory matrix descriptor (tcgen05): start, LBO, SBO (bytes >> 4),
@@ -190,33 +224,61 @@ constexpr uint32_t LAYOUT_NONE = 0;
 // Instruction descriptor of the block-scaled kinds: E2M1 A and B (format 1),
 // both K-major, N >> 3 at bit 17, scale type at bit 23 (1 = UE8M0,
 // 0 = UE4M3), M >> 4 at bit 24, scale-factor byte ids at bits 29 (A) / 4 (B).
-FP4_DEV uint32_t make_idesc(int n, bool ue8m0, uint32_t sfa_id, uint32_t sfb_id) {
+FP4_DEV uint32_t make_idesc(int n, bool ue8m0, uint32_t sfa_id, uint32_t sfb_id, int m = BM) {
     return (sfb_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
-           ((uint32_t)(BM >> 4) << 24) | (sfa_id << 29);
+           ((uint32_t)(m >> 4) << 24) | (sfa_id << 29);
 }
 
+// G = 2: one MMA over the CTA pair (M = 256: A rows from each CTA's shared
+// memory, B split by N halves across the two, D into each CTA's TMEM).
+template <int G = 1>
 FP4_DEV void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
+    if (G == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.u32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.u32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
 }
+template <int G = 1>
 FP4_DEV void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
+    if (G == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.u32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], "
+            "p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.u32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], "
+            "p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
 }
+// one 512-byte scale atom into TMEM, replicated into the four lane quarters
+// (G = 2: in each CTA of the pair, from its own shared memory)
+template <int G = 1>
 FP4_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    if (G == 2)
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // 32 lanes x 32 columns of 32-bit accumulator; the wait is part of the same
 // asm statement, so no use of the registers can be scheduled before it.
@@ -333,11 +395,13 @@ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 // allow (up to MAX_STAGES): the operand loads of the next stages are what
 // hides the L2/HBM latency.  (Halving BK to deepen the ring measured slower:
 // 64-byte rows cost more than the extra depth gains.)
-template <bool NV, int BN, int EPI>
+// P2: the CTA-pair kernel, where each CTA's stage holds its own 128 rows of
+// A, its N-half of the B tile and the scale atoms of the whole B tile.
+template <bool NV, int BN, int EPI, bool P2 = false>
 struct Cfg {
     static constexpr int SF_CHUNKS = NV ? BK / 64 : BK / 128;  // 512-byte atoms per 128 rows per stage
     static constexpr int A_BYTES = BM * BK_BYTES;
-    static constexpr int B_BYTES = BN * BK_BYTES;
+    static constexpr int B_BYTES = (P2 ? BN / 2 : BN) * BK_BYTES;
     static constexpr int SFA_BYTES = SF_CHUNKS * 512;
     static constexpr int SFB_BYTES = (BN / 128) * SF_CHUNKS * 512;
     static constexpr int TX_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // bytes landing per stage
@@ -363,11 +427,15 @@ struct Cfg {
     static_assert(2 * MAX_STAGES * 8 + 64 <= 256, "barrier area");
 };
 
-template <bool NV, int BN, int EPI, int CM>
+template <bool NV, int BN, int EPI, int CM, bool P2 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, KParams p) {
-    using C = Cfg<NV, BN, EPI>;
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
+                    const __grid_constant__ CUtensorMap tmSB, KParams p) {
+    using C = Cfg<NV, BN, EPI, P2>;
+    static_assert(!P2 || (CM == 2 && EPI == EPI_STORE && BN == 256), "pair mode: plain-store 256-wide tiles");
+    constexpr int G = P2 ? 2 : 1;       // tcgen05 CTA group
+    constexpr int MMA_M = P2 ? 2 * BM : BM;
     constexpr int STAGES = C::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -412,24 +480,38 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CM);
+            mbar_init(&empty[s], P2 ? 1 : CM);  // pair: the leader's commit reaches each CTA once
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, EPI_WARPS);
+        mbar_init(acc_empty, P2 ? 2 * EPI_WARPS : EPI_WARPS);  // pair: both CTAs' epilogues, on the leader
         mbar_init(drain_bar, 1);
         mbar_init(epi_bar, EPI_WARPS * 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (P2) {
+            // both CTAs of the pair allocate the same columns together
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     if (warp == 0 && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+        if (P2) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmSA) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmSB) : "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -452,6 +534,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *abort_flag = 1;
                     ok = false;
                     break;
+                }
+                if (P2) {
+                    // this CTA's A rows, its N-half of B, its A scales and the
+                    // whole B tile's scales; completion counted on the leader
+                    const uint32_t fb = mapa_rank(smem_u32(&full[stage]), 0);
+                    if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::TX_BYTES);
+                    tma_load_2d_pair(stage_a(stage), &tmA, kb * BK_BYTES, (int)m0, fb);
+                    tma_load_2d_pair(stage_b(stage), &tmB, kb * BK_BYTES, (int)(n0 + 128 * rank), fb);
+                    tma_load_2d_pair(stage_sfa(stage), &tmSA, 0, (int)((m0 >> 7) * k_atoms + kb * C::SF_CHUNKS), fb);
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        tma_load_2d_pair(stage_sfb(stage) + h * C::SF_CHUNKS * 512, &tmSB, 0,
+                                         (int)(((n0 >> 7) + h) * k_atoms + kb * C::SF_CHUNKS), fb);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    continue;
                 }
                 mbar_expect_tx(&full[stage], C::TX_BYTES);
                 tma_load_2d(stage_a(stage), &tmA, kb * BK_BYTES, (int)m0, &full[stage]);
@@ -480,8 +581,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
-        if (!ok) {
+        if (!ok && (!P2 || rank == 0)) {
             // drain: wait (bounded) for the loads of the stages still in flight
+            // (pair: the leader's barriers count the loads of both CTAs)
             int s = stage;
             uint32_t ph = phase;
             for (int i = 0; i < STAGES && i < issued; ++i) {
@@ -492,8 +594,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_wait(&full[s], ph);
             }
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && (!P2 || rank == 0)) {
         // ------------------------------------------------ MMA issuer ------
+        // (pair: the leader issues for both CTAs)
         const uint32_t sf_base = tmem + SF_COL0;
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
@@ -514,34 +617,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t sfa_col = sf_base + stage * C::SF_COLS;
                 const uint32_t sfb_col = sfa_col + C::SF_COLS_A;
-                // scale atoms -> TMEM (replicated into the four lane quarters)
+                // each chunk's scale atoms go to TMEM (replicated into the four
+                // lane quarters) right before the MMAs that read them
+                const uint32_t a_base = smem_u32(stage_a(stage)), b_base = smem_u32(stage_b(stage));
+                constexpr int MMAS_PER_CHUNK = (BK / 64) / C::SF_CHUNKS;
 #pragma unroll
                 for (int c = 0; c < C::SF_CHUNKS; ++c) {
-                    tc_cp_sf(sfa_col + 4 * c, smem_desc(smem_u32(stage_sfa(stage) + c * 512), 0, 128, LAYOUT_NONE));
+                    tc_cp_sf<G>(sfa_col + 4 * c,
+                                smem_desc(smem_u32(stage_sfa(stage) + c * 512), 0, 128, LAYOUT_NONE));
 #pragma unroll
                     for (int h = 0; h < BN / 128; ++h)
-                        tc_cp_sf(sfb_col + c * (BN / 32) + 4 * h,
-                                 smem_desc(smem_u32(stage_sfb(stage) + (h * C::SF_CHUNKS + c) * 512), 0, 128,
-                                           LAYOUT_NONE));
-                }
-                const uint32_t a_base = smem_u32(stage_a(stage)), b_base = smem_u32(stage_b(stage));
+                        tc_cp_sf<G>(sfb_col + c * (BN / 32) + 4 * h,
+                                    smem_desc(smem_u32(stage_sfb(stage) + (h * C::SF_CHUNKS + c) * 512), 0, 128,
+                                              LAYOUT_NONE));
 #pragma unroll
-                for (int kk = 0; kk < BK / 64; ++kk) {
-                    // each MMA's 64 FP4 values start 32 bytes further into the rows
-                    const uint64_t ad = smem_desc(a_base + kk * 32, 16, AB_SBO, AB_LAYOUT);
-                    const uint64_t bd = smem_desc(b_base + kk * 32, 16, AB_SBO, AB_LAYOUT);
-                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                    if (NV) {
-                        mma_nvf4(tmem, ad, bd, make_idesc(BN, false, 0, 0), sfa_col + 4 * kk, sfb_col + kk * (BN / 32),
-                                 acc);
-                    } else {
-                        const int c = kk >> 1;
-                        const uint32_t sid = (uint32_t)(kk & 1) * 2;
-                        mma_mxf4(tmem, ad, bd, make_idesc(BN, true, sid, sid), sfa_col + 4 * c,
-                                 sfb_col + c * (BN / 32), acc);
+                    for (int q = 0; q < MMAS_PER_CHUNK; ++q) {
+                        const int kk = c * MMAS_PER_CHUNK + q;
+                        // each MMA's 64 FP4 values start 32 bytes further into the rows
+                        const uint64_t ad = smem_desc(a_base + kk * 32, 16, AB_SBO, AB_LAYOUT);
+                        const uint64_t bd = smem_desc(b_base + kk * 32, 16, AB_SBO, AB_LAYOUT);
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        if (NV) {
+                            mma_nvf4<G>(tmem, ad, bd, make_idesc(BN, false, 0, 0, MMA_M), sfa_col + 4 * kk,
+                                        sfb_col + kk * (BN / 32), acc);
+                        } else {
+                            const uint32_t sid = (uint32_t)(kk & 1) * 2;
+                            mma_mxf4<G>(tmem, ad, bd, make_idesc(BN, true, sid, sid, MMA_M), sfa_col + 4 * c,
+                                        sfb_col + c * (BN / 32), acc);
+                        }
                     }
                 }
-                if (CM > 1)
+                if (P2)
+                    tc_commit_mc<2>(&empty[stage], (uint16_t)3);
+                else if (CM > 1)
                     tc_commit_mc(&empty[stage], (uint16_t)((1u << CM) - 1));
                 else
                     tc_commit(&empty[stage]);
@@ -551,12 +659,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok) break;
-            tc_commit(acc_full);
+            if (P2)
+                tc_commit_mc<2>(acc_full, (uint16_t)3);
+            else
+                tc_commit(acc_full);
             acc_phase ^= 1;
         }
         // drain point of everything issued (its own barrier, so that no
         // epilogue wait on acc_full can see an extra phase)
-        tc_commit(drain_bar);
+        tc_commit<G>(drain_bar);
         mbar_wait(drain_bar, 0);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue --------
@@ -591,7 +702,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < NC; ++c) tmem_ld32(lane_base + half * (BN / 2) + 32 * c, r + 32 * c);
                 tc_fence_before();
-                if (lane == 0) mbar_arrive(acc_empty);
+                if (lane == 0) {
+                    if (P2 && rank != 0)
+                        mbar_arrive_cluster(mapa_rank(smem_u32(acc_empty), 0));
+                    else
+                        mbar_arrive(acc_empty);
+                }
                 float sa = 1.0f;
                 if (NV) sa = __fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]);
                 const bool tma_out = p.beta == 0.0f || p.beta == 1.0f;
@@ -845,7 +961,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (CM > 1) cluster_sync();  // no peer still multicasts into this CTA
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+        if (P2)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                         : "memory");
     }
 }
 
@@ -878,6 +999,20 @@ bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K) {
     return r == CUDA_SUCCESS;
 }
 
+// Scale atoms [atoms][512 bytes] as a 2D uint32 tensor, box = `chunk`
+// consecutive atoms (the pair kernel loads its scales through TMA so that
+// their completion can be counted on the pair leader's barrier).
+bool make_sf_map(CUtensorMap* map, const void* scales, int64_t atoms, int chunk) {
+    cuuint64_t dims[2] = {128u, (cuuint64_t)atoms};
+    cuuint64_t strides[1] = {512u};
+    cuuint32_t box[2] = {128u, (cuuint32_t)chunk};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(scales), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Row-major output [M][N] (fp32 or bf16), box 128 bytes x 32 rows, 128B swizzle.
 bool make_out_map(CUtensorMap* map, void* c, int64_t M, int64_t N, int out_dtype) {
     const bool f32 = out_dtype == FP4_OUT_F32;
@@ -905,15 +1040,23 @@ int sm_count() {
     return cached[dev];
 }
 
-template <bool NV, int BN, int EPI, int CM>
+template <bool NV, int BN, int EPI, int CM, bool P2 = false>
 int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream_t stream) {
-    using C = Cfg<NV, BN, EPI>;
-    CUtensorMap ta, tb, tc;
+    using C = Cfg<NV, BN, EPI, P2>;
+    CUtensorMap ta, tb, tc, tsa, tsb;
     if (!make_map(&ta, g.a_codes, g.M, g.K) || !make_map(&tb, g.b_codes, g.b_rows, g.K)) return FP4_ERR_CUDA;
     memset(&tc, 0, sizeof tc);
+    memset(&tsa, 0, sizeof tsa);
+    memset(&tsb, 0, sizeof tsb);
+    if (P2) {
+        const int64_t k_atoms = NV ? g.K / 64 : g.K / 128;
+        if (!make_sf_map(&tsa, g.a_scales, (g.M / 128) * k_atoms, C::SF_CHUNKS) ||
+            !make_sf_map(&tsb, g.b_scales, (g.b_rows / 128) * k_atoms, C::SF_CHUNKS))
+            return FP4_ERR_CUDA;
+    }
     if (EPI == EPI_STORE && (g.beta == 0.0f || g.beta == 1.0f) && !make_out_map(&tc, g.c, g.M, g.N, g.out_dtype))
         return FP4_ERR_CUDA;
-    auto kern = fp4_gemm_kernel<NV, BN, EPI, CM>;
+    auto kern = fp4_gemm_kernel<NV, BN, EPI, CM, P2>;
     int dev = 0;
     cudaGetDevice(&dev);
     static bool attr_done[64] = {};
@@ -944,7 +1087,7 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
     }
     const int64_t clusters = n_units < max_clusters ? n_units : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * CM));
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp) != cudaSuccess) return FP4_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsa, tsb, kp) != cudaSuccess) return FP4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -1003,12 +1146,14 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     const bool wide = (g.N % 256) == 0;
     const int64_t units_1 = (g.M / BM) * (g.N / (wide ? 256 : 128));
     if (g.nv) {
+        // NVFP4 stays on the CTA-multicast kernel: its twice-as-many scale copies made
+        // the pair kernel slower there (measured), while MXFP4 gains 5-10% from it
         if (wide) return pair ? launch_t<true, 256, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
                               : launch_t<true, 256, EPI_STORE, 1>(g, kp, units_1, stream);
         return pair ? launch_t<true, 128, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
                     : launch_t<true, 128, EPI_STORE, 1>(g, kp, units_1, stream);
     }
-    if (wide) return pair ? launch_t<false, 256, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+    if (wide) return pair ? launch_t<false, 256, EPI_STORE, 2, true>(g, kp, units_1 / 2, stream)
                           : launch_t<false, 256, EPI_STORE, 1>(g, kp, units_1, stream);
     return pair ? launch_t<false, 128, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
                 : launch_t<false, 128, EPI_STORE, 1>(g, kp, units_1, stream);

@@ -37,7 +37,7 @@ constexpr int LDS = TILE + PAD;      // smem row stride (elements)
 constexpr int THREADS = 256;
 
 struct SmemQ {
-    uint16_t tile[TILE * LDS];       // 34,816 B
+    uint16_t tile[2][TILE * LDS];    // 2 x 34,816 B: the tile being encoded and the next one landing
     uint8_t row_codes[TILE * 64];    // 8 KB staged row-view codes
     uint8_t col_codes[TILE * 64];    // 8 KB staged column-view codes
     uint8_t row_sc[1024];            // staged scale atoms (1 MX / 2 NV)
@@ -62,12 +62,6 @@ FP4_DEV uint32_t amax_bits32(const float* v) {
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-    return m;
-}
-FP4_DEV uint32_t amax_bits16(const float* v) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
     return m;
 }
 // Packed per-half maximum of |bf16| over n bf16x2 words (bits of the low and
@@ -234,17 +228,15 @@ FP4_DEV void unpack_lane(const uint32_t* w, int h, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
 }
 
+// Encode the 128x128 tile (ty, tx), already in shared memory at `tbuf`, into
+// both views: steps 2-5 below.  Called by all threads of the CTA with the
+// tile visible to every thread.
 template <bool NV>
-__global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
+FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, int64_t ty, int64_t tx) {
     const int t = threadIdx.x;
-    const int64_t r0 = (int64_t)blockIdx.y * TILE, c0 = (int64_t)blockIdx.x * TILE;
+    const int64_t r0 = ty * TILE, c0 = tx * TILE;
     const bool w2d = (p.flags & FP4_FLAG_WEIGHT_2D) != 0;
     const bool do_row = (p.views & FP4_VIEW_ROW) != 0, do_col = (p.views & FP4_VIEW_COL) != 0;
-
-    // 1. tile -> shared memory (16-byte coalesced loads, optional pre-op)
-    load_tile(p, r0, c0, s.tile, true);
 
     // outer factors of this tile's row strip / column strip
     float senc_row = 1.0f, senc_col = 1.0f;
@@ -253,20 +245,19 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p
         if (p.route == FP4_ROUTE_NVFP4_GLOBAL || w2d) {
             senc_row = senc_col = nv_senc(__uint_as_float(ws[0]));
         } else {
-            senc_row = nv_senc(__uint_as_float(ws[1 + blockIdx.y]));
-            senc_col = nv_senc(__uint_as_float(ws[1 + (p.R >> 7) + blockIdx.x]));
+            senc_row = nv_senc(__uint_as_float(ws[1 + ty]));
+            senc_col = nv_senc(__uint_as_float(ws[1 + (p.R >> 7) + tx]));
         }
         if (t == 0) {
             if (p.route == FP4_ROUTE_NVFP4_LOCAL && !w2d) {
-                if (do_row && blockIdx.x == 0) p.row_outer[blockIdx.y] = senc_row;
-                if (do_col && blockIdx.y == 0) p.col_outer[blockIdx.x] = senc_col;
-            } else if (blockIdx.x == 0 && blockIdx.y == 0) {
+                if (do_row && tx == 0) p.row_outer[ty] = senc_row;
+                if (do_col && ty == 0) p.col_outer[tx] = senc_col;
+            } else if (tx == 0 && ty == 0) {
                 if (do_row) p.row_outer[0] = senc_row;
                 if (do_col) p.col_outer[0] = senc_col;
             }
         }
     }
-    __syncthreads();
 
     // 2. shared 2D weight scales: the maxima of the 16-value pieces of every
     //    row (16-byte shared loads), then one reduction per tile
@@ -274,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {
             const int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
-            const uint16_t* src = &s.tile[r * LDS + j * 32];
+            const uint16_t* src = &tbuf[r * LDS + j * 32];
             uint32_t w[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -329,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p
         for (int k = 0; k < 2; ++k) {
             const int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
             uint32_t w[16];
-            const uint16_t* src = &s.tile[r * LDS + j * 32];
+            const uint16_t* src = &tbuf[r * LDS + j * 32];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
@@ -381,7 +372,7 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p
         const int cp = t & 63, j = t >> 6;
         uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&s.tile[(j * 32 + i) * LDS + 2 * cp]);
+        for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tbuf[(j * 32 + i) * LDS + 2 * cp]);
         if (had) {
             // the sign of position i (mod 16) applies to both columns of the pair
 #pragma unroll
@@ -463,6 +454,58 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p
     }
 }
 
+// Asynchronous 16-byte global -> shared copies (bypassing L1).
+FP4_DEV void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+FP4_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+FP4_DEV void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Start loading the 128x128 tile at (r0, c0) into `tile` (row stride LDS).
+FP4_DEV void prefetch_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* tile) {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int q = t + i * THREADS;
+        cp_async16(&tile[(q >> 4) * LDS + (q & 15) * 8], p.x + (r0 + (q >> 4)) * p.ld + c0 + (q & 15) * 8);
+    }
+}
+
+// Each CTA walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... (row-strip-major
+// order) with two tile buffers: while one tile is encoded the next one is
+// already in flight, so its load latency hides behind the encoding.  With an
+// RMSNorm pre-op the tile is loaded (and transformed) synchronously.
+template <bool NV>
+__global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
+    const int64_t tiles_x = p.C / TILE, n_tiles = tiles_x * (p.R / TILE);
+    const bool async = p.pre == PRE_NONE;
+    int64_t tile = blockIdx.x;
+    if (tile >= n_tiles) return;
+    if (async) {
+        prefetch_tile(p, (tile / tiles_x) * TILE, (tile % tiles_x) * TILE, s.tile[0]);
+        cp_async_commit();
+    }
+    for (int it = 0; tile < n_tiles; tile += gridDim.x, ++it) {
+        uint16_t* cur = s.tile[it & 1];
+        const int64_t ty = tile / tiles_x, tx = tile % tiles_x;
+        if (async) {
+            const int64_t next = tile + gridDim.x;
+            if (next < n_tiles) prefetch_tile(p, (next / tiles_x) * TILE, (next % tiles_x) * TILE, s.tile[(it + 1) & 1]);
+            cp_async_commit();    // one group per iteration (possibly empty)
+            cp_async_wait_prev(); // this thread's copies of the current tile have landed
+        } else {
+            load_tile(p, ty * TILE, tx * TILE, cur, true);
+        }
+        __syncthreads();
+        encode_tile<NV>(p, s, cur, ty, tx);
+        __syncthreads();  // staging buffers and `cur` are free for the next tile
+    }
+}
+
 // Tile-amax pre-pass for NVFP4: max |x| of each 128x128 tile folded into the
 // tensor slot ws[0], the tile's row-strip slot and its column-strip slot.
 __global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
@@ -506,8 +549,16 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
 
 }  // namespace
 
+// CTAs of the encoder: two tiles per CTA, so that the second tile's load
+// overlaps the first one's encoding.  (Measured against one tile per CTA and
+// against one CTA per resident slot looping over all tiles: two per CTA was
+// as fast as the former on the SR + H32 gradient and as fast as the latter on
+// the latency-bound weight and activation producers.)
+unsigned encoder_grid(int64_t n_tiles) { return (unsigned)((n_tiles + 1) / 2); }
+
 int launch_quantize(const QuantParams& p, cudaStream_t stream) {
     dim3 grid((unsigned)(p.C / TILE), (unsigned)(p.R / TILE));
+    const int64_t n_tiles = (p.C / TILE) * (p.R / TILE);
     const size_t smem = sizeof(SmemQ);
     const bool nv = p.route != FP4_ROUTE_MXFP4;
     if (nv) {
@@ -522,7 +573,7 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
             cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             attr_nv = true;
         }
-        quantize_tile_kernel<true><<<grid, THREADS, smem, stream>>>(p);
+        quantize_tile_kernel<true><<<encoder_grid(n_tiles), THREADS, smem, stream>>>(p);
     } else {
         static bool attr_mx = false;
         if (!attr_mx) {
@@ -530,7 +581,7 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
             cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             attr_mx = true;
         }
-        quantize_tile_kernel<false><<<grid, THREADS, smem, stream>>>(p);
+        quantize_tile_kernel<false><<<encoder_grid(n_tiles), THREADS, smem, stream>>>(p);
     }
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
