@@ -320,10 +320,15 @@ def run_ours(args):
             tf = gemm_flops / (v * 1e-3) / 1e12
             kernels[n] = {"ms": round(v, 4), "TFLOP/s": round(tf, 1), "fp4_frac": round(tf / fp4_peak, 4)}
 
+    # the operand-wise hybrid on the same tensors (MXFP4 Fprop and Wgrad with
+    # plain H16 on the pair, CTA-local NVFP4 Dgrad with row SR)
+    hybrid = None if args.no_legs else run_hybrid_leg(X, W, DY, peaks)
     # free the main workload's buffers before the other legs
     del X, W, DY, Y, DX, DW, xr, xc, wr, wc, dr, dc, dX2, dW2, dDY2
     torch.cuda.empty_cache()
     legs = {} if args.no_legs else run_legs(args, peaks)
+    if hybrid is not None:
+        legs = {"operand_hybrid_h16_w1": hybrid, **legs}
     cpu = cpu_baseline_sample(seconds_target=args.cpu_seconds) if args.cpu_seconds > 0 else None
     line = {
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -351,6 +356,64 @@ def run_ours(args):
 
 
 # ------------------------------------------------------------ other legs ----
+def run_hybrid_leg(X, W, DY, peaks, steps: int = 10, warmup: int = 3) -> dict:
+    """One pass of the operand-wise hybrid boundary over the W1-shaped tensors:
+    the three producers (X: MXFP4 both views, plain H16 on the column view;
+    W: MXFP4 2D32 row view + CTA-local 2D16 column view; dY: CTA-local row
+    view with SR + MXFP4 column view with plain H16) and the three GEMMs."""
+    import torch
+    import fp4_quantized_linears_gb300 as F
+    T_, di = X.shape
+    do = W.shape[0]
+    ones = [1] * 16
+    h16 = F.FP4_FLAG_HADAMARD16_COL
+    xr, xc = F.alloc_view("mx", T_, di), F.alloc_view("mx", di, T_)
+    wr, wc = F.alloc_view("mx", do, di, F.FP4_FLAG_WEIGHT_2D), F.alloc_view("nv_local", di, do, F.FP4_FLAG_WEIGHT_2D)
+    dr, dc = F.alloc_view("nv_local", T_, do), F.alloc_view("mx", do, T_)
+    ws = torch.empty(max(F.fp4_quantize_hybrid_workspace_bytes("nv_local", "mx", T_, do, 3, h16),
+                         F.fp4_quantize_hybrid_workspace_bytes("mx", "nv_local", do, di, 3, F.FP4_FLAG_WEIGHT_2D), 16),
+                     dtype=torch.uint8, device=X.device)
+    Y = torch.empty((T_, do), dtype=torch.float32, device=X.device)
+    DX = torch.empty((T_, di), dtype=torch.float32, device=X.device)
+    DW = torch.empty((do, di), dtype=torch.float32, device=X.device)
+    names = ["quant_x", "quant_w", "quant_dy", "fprop", "dgrad", "wgrad"]
+
+    def step(ev=None, i=0):
+        def mark(k):
+            if ev is not None:
+                ev[k].record()
+        mark(0)
+        F.fp4_quantize(X, "mx", 3, h16, hadamard_signs=ones, row_out=xr, col_out=xc)
+        mark(1)
+        F.fp4_quantize_hybrid(W, "mx", "nv_local", 3, F.FP4_FLAG_WEIGHT_2D, row_out=wr, col_out=wc, workspace=ws)
+        mark(2)
+        F.fp4_quantize_hybrid(DY, "nv_local", "mx", 3, F.FP4_FLAG_SR_ROW | h16, sr_seed=4, sr_offset=i,
+                              hadamard_signs=ones, row_out=dr, col_out=dc, workspace=ws)
+        mark(3)
+        F.fp4_linear_fprop(xr, wr, Y)
+        mark(4)
+        F.fp4_linear_dgrad(dr, wc, DX)
+        mark(5)
+        F.fp4_linear_wgrad(dc, xc, DW)
+        mark(6)
+
+    for i in range(warmup):
+        step(i=i)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for i in range(steps):
+        step(evs[i], 100 + i)
+    torch.cuda.synchronize()
+    if F.fp4_status() != F.FP4_OK:
+        raise RuntimeError("device status set in the hybrid leg")
+    per = {n: statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(steps))
+           for k, n in enumerate(names)}
+    ms = sum(per.values())
+    fl = 3 * 2.0 * T_ * di * do
+    return {"ms_per_step": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
+            "kernels_ms": {k: round(v, 4) for k, v in per.items()}}
+
+
 def _timed(fn, steps: int, warmup: int) -> float:
     """Mean device milliseconds of fn() over `steps` calls after `warmup`."""
     import torch

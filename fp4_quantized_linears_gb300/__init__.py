@@ -40,6 +40,7 @@ FP4_VIEW_COL = 2
 FP4_FLAG_WEIGHT_2D = 1
 FP4_FLAG_SR_ROW = 2
 FP4_FLAG_HADAMARD_COL = 4
+FP4_FLAG_HADAMARD16_COL = 8
 
 FP4_OUT_F32 = 0
 FP4_OUT_BF16 = 1
@@ -98,6 +99,11 @@ def _declare(L):
                                                         ctypes.POINTER(c_sz)]),
         "fp4_quantize": (ctypes.c_int, [vp, c_i64, c_i64, c_i64, ctypes.c_int, ctypes.c_uint, ctypes.c_uint, c_u64,
                                         c_u64, ctypes.POINTER(ctypes.c_int8), tp, tp, vp, c_sz, vp]),
+        "fp4_quantize_hybrid": (ctypes.c_int, [vp, c_i64, c_i64, c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint,
+                                               ctypes.c_uint, c_u64, c_u64, ctypes.POINTER(ctypes.c_int8), tp, tp, vp,
+                                               c_sz, vp]),
+        "fp4_quantize_hybrid_workspace_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, c_i64, c_i64,
+                                                               ctypes.c_uint, ctypes.c_uint, ctypes.POINTER(c_sz)]),
         "fp4_linear_fprop": (ctypes.c_int, [tp, tp, vp, ctypes.c_int, ctypes.c_float, vp]),
         "fp4_linear_dgrad": (ctypes.c_int, [tp, tp, vp, ctypes.c_int, ctypes.c_float, vp]),
         "fp4_linear_wgrad": (ctypes.c_int, [tp, tp, vp, ctypes.c_float, vp]),
@@ -186,18 +192,42 @@ def fp4_quantize(x: torch.Tensor, route, views: int = FP4_VIEW_ROW | FP4_VIEW_CO
     """Quantize a bf16 CUDA tensor [rows, cols] into the requested views.
 
     Returns (row_view or None, col_view or None)."""
+    return _quantize(x, route, route, False, views, flags, sr_seed, sr_offset, hadamard_signs, row_out, col_out,
+                     workspace, stream)
+
+
+def fp4_quantize_hybrid(x: torch.Tensor, row_route, col_route, views: int = FP4_VIEW_ROW | FP4_VIEW_COL,
+                        flags: int = 0, sr_seed: int = 0, sr_offset: int = 0, hadamard_signs=None,
+                        row_out: QView | None = None, col_out: QView | None = None,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """The operand-wise hybrid producer: the row view under row_route and the
+    column view under col_route from one read of x.  Returns (row_view, col_view)."""
+    return _quantize(x, row_route, col_route, True, views, flags, sr_seed, sr_offset, hadamard_signs, row_out,
+                     col_out, workspace, stream)
+
+
+def fp4_quantize_hybrid_workspace_bytes(row_route, col_route, rows: int, cols: int, views: int = 3,
+                                        flags: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fp4_quantize_hybrid_workspace_bytes(_route(row_route), _route(col_route), rows, cols, views, flags,
+                                                      ctypes.byref(n)), "fp4_quantize_hybrid_workspace_bytes")
+    return n.value
+
+
+def _quantize(x, row_route, col_route, hybrid, views, flags, sr_seed, sr_offset, hadamard_signs, row_out, col_out,
+              workspace, stream):
     L = load()
-    r = _route(route)
+    rr, cr = _route(row_route), _route(col_route)
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda:
         raise ValueError("x must be a 2D bfloat16 CUDA tensor")
     if x.stride(1) != 1:
         raise ValueError("x must have unit stride along columns")
     R, C = x.shape
     if views & FP4_VIEW_ROW and row_out is None:
-        row_out = alloc_view(r, R, C, flags, x.device)
+        row_out = alloc_view(rr, R, C, flags, x.device)
     if views & FP4_VIEW_COL and col_out is None:
-        col_out = alloc_view(r, C, R, flags, x.device)
-    need = fp4_quantize_workspace_bytes(r, R, C, views, flags)
+        col_out = alloc_view(cr, C, R, flags, x.device)
+    need = fp4_quantize_hybrid_workspace_bytes(rr, cr, R, C, views, flags)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     signs = None
@@ -206,11 +236,16 @@ def fp4_quantize(x: torch.Tensor, route, views: int = FP4_VIEW_ROW | FP4_VIEW_CO
         signs = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int8))
     rs = row_out.struct() if row_out is not None else None
     cs = col_out.struct() if col_out is not None else None
-    code = L.fp4_quantize(ctypes.c_void_p(x.data_ptr()), R, C, x.stride(0), r, views, flags, sr_seed, sr_offset,
-                          signs, ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None,
-                          ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None,
-                          workspace.numel() if workspace is not None else 0, _stream(stream))
-    _check(code, "fp4_quantize")
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    ws_n = workspace.numel() if workspace is not None else 0
+    args = (signs, ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None, ws_ptr, ws_n, _stream(stream))
+    if hybrid:
+        code = L.fp4_quantize_hybrid(ctypes.c_void_p(x.data_ptr()), R, C, x.stride(0), rr, cr, views, flags, sr_seed,
+                                     sr_offset, *args)
+    else:
+        code = L.fp4_quantize(ctypes.c_void_p(x.data_ptr()), R, C, x.stride(0), rr, views, flags, sr_seed, sr_offset,
+                              *args)
+    _check(code, "fp4_quantize_hybrid" if hybrid else "fp4_quantize")
     if rs:
         row_out.rows, row_out.cols, row_out.route, row_out.outer_count = rs.rows, rs.cols, rs.route, rs.outer_count
     if cs:

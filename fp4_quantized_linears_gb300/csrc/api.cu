@@ -61,66 +61,70 @@ int fp4_tensor_bytes(int route, int64_t rows, int64_t cols, unsigned flags, size
 
 int fp4_quantize_workspace_bytes(int route, int64_t rows, int64_t cols, unsigned views, unsigned flags,
                                  size_t* bytes) {
-    (void)views;
-    (void)flags;
-    if (!route_ok(route) || !bytes || rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;
+    return fp4_quantize_hybrid_workspace_bytes(route, route, rows, cols, views, flags, bytes);
+}
+
+int fp4_quantize_hybrid_workspace_bytes(int row_route, int col_route, int64_t rows, int64_t cols, unsigned views,
+                                        unsigned flags, size_t* bytes) {
+    if (!route_ok(row_route) || !route_ok(col_route) || !bytes || rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;
     if (rows % 128 || cols % 128) return FP4_ERR_UNSUPPORTED_SHAPE;
-    *bytes = route == FP4_ROUTE_MXFP4 ? 0 : (size_t)(1 + rows / 128 + cols / 128) * 4;
+    *bytes = quant_workspace_slots(rows, cols, row_route, col_route, views ? views : 3u, flags) * 4;
     return FP4_OK;
 }
 
 // Validate a quantizer call and fill its parameters; nothing is enqueued.
 // x may be NULL when the caller produces it in an earlier kernel (pre-ops).
-static int prepare_quant(const void* x, bool x_from_pre, int64_t rows, int64_t cols, int64_t ld, int route,
-                         unsigned views, unsigned flags, uint64_t sr_seed, uint64_t sr_offset,
+static int prepare_quant(const void* x, bool x_from_pre, int64_t rows, int64_t cols, int64_t ld, int row_route,
+                         int col_route, unsigned views, unsigned flags, uint64_t sr_seed, uint64_t sr_offset,
                          const int8_t* hadamard_signs, fp4_tensor* row_out, fp4_tensor* col_out, void* workspace,
                          size_t workspace_bytes, QuantParams* p) {
-    if (!route_ok(route)) return FP4_ERR_INVALID_ARG;
-    if ((views & ~3u) || views == 0 || (flags & ~7u)) return FP4_ERR_INVALID_ARG;
+    if (!route_ok(row_route) || !route_ok(col_route)) return FP4_ERR_INVALID_ARG;
+    if ((views & ~3u) || views == 0 || (flags & ~15u)) return FP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0 || ld < cols) return FP4_ERR_INVALID_ARG;
     if (rows % 128 || cols % 128) return FP4_ERR_UNSUPPORTED_SHAPE;
-    if ((flags & FP4_FLAG_WEIGHT_2D) && (flags & (FP4_FLAG_SR_ROW | FP4_FLAG_HADAMARD_COL)))
-        return FP4_ERR_ROUTE_MISMATCH;
-    if ((flags & FP4_FLAG_HADAMARD_COL) && route != FP4_ROUTE_MXFP4) return FP4_ERR_ROUTE_MISMATCH;
+    const unsigned had_any = FP4_FLAG_HADAMARD_COL | FP4_FLAG_HADAMARD16_COL;
+    if ((flags & FP4_FLAG_WEIGHT_2D) && (flags & (FP4_FLAG_SR_ROW | had_any))) return FP4_ERR_ROUTE_MISMATCH;
+    if ((flags & FP4_FLAG_HADAMARD_COL) && (flags & FP4_FLAG_HADAMARD16_COL)) return FP4_ERR_INVALID_ARG;
+    if ((flags & FP4_FLAG_HADAMARD_COL) && col_route != FP4_ROUTE_MXFP4) return FP4_ERR_ROUTE_MISMATCH;
     const bool do_row = views & FP4_VIEW_ROW, do_col = views & FP4_VIEW_COL;
     if ((do_row && !row_out) || (do_col && !col_out)) return FP4_ERR_INVALID_ARG;
     for (int v = 0; v < 2; ++v) {
         fp4_tensor* t = v == 0 ? (do_row ? row_out : nullptr) : (do_col ? col_out : nullptr);
         if (!t) continue;
         if (!t->codes || !t->scales || !aligned16(t->codes) || !aligned16(t->scales)) return FP4_ERR_INVALID_ARG;
-        if (route != FP4_ROUTE_MXFP4 && !t->outer) return FP4_ERR_INVALID_ARG;
+        if ((v == 0 ? row_route : col_route) != FP4_ROUTE_MXFP4 && !t->outer) return FP4_ERR_INVALID_ARG;
     }
     uint32_t sign_mask = 0;
-    if (flags & FP4_FLAG_HADAMARD_COL) {
+    if (flags & had_any) {
         if (!hadamard_signs) return FP4_ERR_INVALID_ARG;
         for (int j = 0; j < 16; ++j) {
             if (hadamard_signs[j] != 1 && hadamard_signs[j] != -1) return FP4_ERR_INVALID_ARG;
             if (hadamard_signs[j] < 0) sign_mask |= 1u << j;
         }
     }
-    size_t need = 0;
-    fp4_quantize_workspace_bytes(route, rows, cols, views, flags, &need);
+    const size_t need = quant_workspace_slots(rows, cols, row_route, col_route, views, flags) * 4;
     if (need > 0 && (!workspace || workspace_bytes < need)) return FP4_ERR_WORKSPACE;
     if (rows > 0 && cols > 0 && !x_from_pre && (!x || !aligned16(x) || ld % 8)) return FP4_ERR_INVALID_ARG;
 
     if (do_row) {
         row_out->rows = rows;
         row_out->cols = cols;
-        row_out->route = route;
-        row_out->outer_count = outer_count_of(route, rows, flags);
+        row_out->route = row_route;
+        row_out->outer_count = outer_count_of(row_route, rows, flags);
     }
     if (do_col) {
         col_out->rows = cols;
         col_out->cols = rows;
-        col_out->route = route;
-        col_out->outer_count = outer_count_of(route, cols, flags);
+        col_out->route = col_route;
+        col_out->outer_count = outer_count_of(col_route, cols, flags);
     }
     *p = QuantParams{};
     p->x = static_cast<const uint16_t*>(x);
     p->R = rows;
     p->C = cols;
     p->ld = ld;
-    p->route = route;
+    p->row_route = row_route;
+    p->col_route = col_route;
     p->views = views;
     p->flags = flags;
     p->seed = sr_seed;
@@ -144,8 +148,19 @@ int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int rout
                  uint64_t sr_seed, uint64_t sr_offset, const int8_t* hadamard_signs, fp4_tensor* row_out,
                  fp4_tensor* col_out, void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
     QuantParams p;
-    int rc = prepare_quant(x, false, rows, cols, ld, route, views, flags, sr_seed, sr_offset, hadamard_signs, row_out,
-                           col_out, workspace, workspace_bytes, &p);
+    int rc = prepare_quant(x, false, rows, cols, ld, route, route, views, flags, sr_seed, sr_offset, hadamard_signs,
+                           row_out, col_out, workspace, workspace_bytes, &p);
+    if (rc != FP4_OK || rows == 0 || cols == 0) return rc;
+    return launch_quantize(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp4_quantize_hybrid(const void* x, int64_t rows, int64_t cols, int64_t ld, int row_route, int col_route,
+                        unsigned views, unsigned flags, uint64_t sr_seed, uint64_t sr_offset,
+                        const int8_t* hadamard_signs, fp4_tensor* row_out, fp4_tensor* col_out, void* workspace,
+                        size_t workspace_bytes, fp4_stream_t stream) {
+    QuantParams p;
+    int rc = prepare_quant(x, false, rows, cols, ld, row_route, col_route, views, flags, sr_seed, sr_offset,
+                           hadamard_signs, row_out, col_out, workspace, workspace_bytes, &p);
     if (rc != FP4_OK || rows == 0 || cols == 0) return rc;
     return launch_quantize(p, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -155,8 +170,8 @@ int fp4_residual_rmsnorm_fwd(int route, unsigned views, const void* r, const voi
                              fp4_tensor* y_col, void* y_tap, void* workspace, size_t workspace_bytes,
                              fp4_stream_t stream) {
     QuantParams p;
-    int rc = prepare_quant(r_out, true, rows, cols, cols, route, views, 0, 0, 0, nullptr, y_row, y_col, workspace,
-                           workspace_bytes, &p);
+    int rc = prepare_quant(r_out, true, rows, cols, cols, route, route, views, 0, 0, 0, nullptr, y_row, y_col,
+                           workspace, workspace_bytes, &p);
     if (rc != FP4_OK || rows == 0 || cols == 0) return rc;
     if (ld < cols || ld % 8) return FP4_ERR_INVALID_ARG;
     if (!r || !g || !r_out || !rstd || !aligned16(r) || !aligned16(g) || !aligned16(r_out) || (b && !aligned16(b)) ||
@@ -196,8 +211,8 @@ int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, 
     if (rows > 0 && cols > 0 && (!workspace || workspace_bytes < need)) return FP4_ERR_WORKSPACE;
     void* qws = workspace ? static_cast<uint8_t*>(workspace) + stats : nullptr;
     QuantParams p;
-    int rc = prepare_quant(dy, false, rows, cols, cols, route, views, sr ? FP4_FLAG_SR_ROW : 0, sr_seed, sr_offset,
-                           nullptr, dr_row, dr_col, qws, workspace ? workspace_bytes - stats : 0, &p);
+    int rc = prepare_quant(dy, false, rows, cols, cols, route, route, views, sr ? FP4_FLAG_SR_ROW : 0, sr_seed,
+                           sr_offset, nullptr, dr_row, dr_col, qws, workspace ? workspace_bytes - stats : 0, &p);
     if (rc != FP4_OK || rows == 0 || cols == 0) return rc;
     if (!r_prime || !rstd || !g || !dr || !aligned16(r_prime) || !aligned16(g) || !aligned16(dr) ||
         (dres && !aligned16(dres)))

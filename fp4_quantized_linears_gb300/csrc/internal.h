@@ -12,17 +12,18 @@ namespace fp4 {
 struct QuantParams {
     const uint16_t* x;  // bf16 [R][ld]
     int64_t R, C, ld;
-    int route;
+    int row_route, col_route;  // FP4_ROUTE_* of each view (they differ in the operand-wise hybrid)
     unsigned views, flags;
     uint64_t seed, offset;
-    uint32_t sign_mask;  // bit j set: sign j of the H32 diagonal is -1
+    uint32_t sign_mask;  // bit j set: sign j of the H32 / H16 diagonal is -1
     uint8_t* row_codes;
     uint8_t* row_scales;
     float* row_outer;
     uint8_t* col_codes;
     uint8_t* col_scales;
     float* col_outer;
-    uint32_t* amax_ws;  // NVFP4: [1 + R/128 + C/128] amax bit slots
+    uint32_t* amax_ws;  // NVFP4: amax bit slots [tensor, R/128 row strips, C/128 column strips,
+                        // (H16 NVFP4 column view) transformed tensor]
     // Optional element-wise pre-op applied while the tile is loaded (the
     // residual-RMSNorm producer, Sec. 3.2):
     //   PRE_RMSNORM_FWD  x = r',  value = bf16(fl32(fl32(r' * rstd[r]) * g[c]))
@@ -45,6 +46,8 @@ int launch_rmsnorm_bwd_stats(const uint16_t* dy, const uint16_t* rp, const float
                              int64_t C, float* mean_g, cudaStream_t stream);
 
 int launch_quantize(const QuantParams& p, cudaStream_t stream);
+// amax slots (4 bytes each) a quantizer call needs in its workspace
+size_t quant_workspace_slots(int64_t R, int64_t C, int row_route, int col_route, unsigned views, unsigned flags);
 int quant_status(cudaStream_t stream, int* code, bool reset);
 
 // C[M][N] = alpha(m,n) * A_hat[M][K] . B_hat[N][K]^T + beta * C

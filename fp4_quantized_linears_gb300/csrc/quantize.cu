@@ -64,6 +64,12 @@ FP4_DEV uint32_t amax_bits32(const float* v) {
     for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
     return m;
 }
+FP4_DEV uint32_t amax_bits16(const float* v) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    return m;
+}
 // Packed per-half maximum of |bf16| over n bf16x2 words (bits of the low and
 // high halves' maxima in the two 16-bit lanes).
 template <int N>
@@ -133,6 +139,25 @@ FP4_DEV void hadamard32_nosign(float* v) {
     const float s = __uint_as_float(0x3E3504F3u);  // fl32(1 / sqrt(32))
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], s);
+}
+
+// H16 butterflies on each 16-value half of 32 registers whose fixed signs
+// were already applied: stages of stride 1, 2, 4, 8, then the multiply by
+// 1/sqrt(16) = 0.25 (exact).
+FP4_DEV void hadamard16x2_nosign(float* v) {
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if ((j & h) == 0) {
+                float a = v[j], b = v[j + h];
+                v[j] = __fadd_rn(a, b);
+                v[j + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], 0.25f);
 }
 
 // Load the 128x128 tile at (r0, c0) into shared memory (row stride LDS),
@@ -229,32 +254,49 @@ FP4_DEV void unpack_lane(const uint32_t* w, int h, float* v) {
 }
 
 // Encode the 128x128 tile (ty, tx), already in shared memory at `tbuf`, into
-// both views: steps 2-5 below.  Called by all threads of the CTA with the
-// tile visible to every thread.
-template <bool NV>
+// both views: steps 2-5 below.  NVR / NVC: the row / column view is NVFP4
+// (else MXFP4); the two differ in the operand-wise hybrid producer.  Called
+// by all threads of the CTA with the tile visible to every thread.
+template <bool NVR, bool NVC>
 FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, int64_t ty, int64_t tx) {
     const int t = threadIdx.x;
     const int64_t r0 = ty * TILE, c0 = tx * TILE;
     const bool w2d = (p.flags & FP4_FLAG_WEIGHT_2D) != 0;
+    const bool h16 = (p.flags & FP4_FLAG_HADAMARD16_COL) != 0;
     const bool do_row = (p.views & FP4_VIEW_ROW) != 0, do_col = (p.views & FP4_VIEW_COL) != 0;
 
-    // outer factors of this tile's row strip / column strip
-    float senc_row = 1.0f, senc_col = 1.0f;
-    if (NV) {
+    // outer factors of this tile's row strip / column strip, per view route:
+    // the tensor factor (ws[0]) for 2D weights and global NVFP4, the strip
+    // factor for CTA-local NVFP4; an H16 column view takes the factors of
+    // the transformed values (column strips, and the last slot for global)
+    float senc_row = 1.0f, senc_col = 1.0f, senc_w = 1.0f;
+    if (NVR || NVC) {
         const uint32_t* ws = p.amax_ws;
-        if (p.route == FP4_ROUTE_NVFP4_GLOBAL || w2d) {
-            senc_row = senc_col = nv_senc(__uint_as_float(ws[0]));
-        } else {
-            senc_row = nv_senc(__uint_as_float(ws[1 + ty]));
-            senc_col = nv_senc(__uint_as_float(ws[1 + (p.R >> 7) + tx]));
+        senc_w = nv_senc(__uint_as_float(ws[0]));
+        if (NVR)
+            senc_row = (w2d || p.row_route == FP4_ROUTE_NVFP4_GLOBAL) ? senc_w : nv_senc(__uint_as_float(ws[1 + ty]));
+        if (NVC) {
+            if (w2d)
+                senc_col = senc_w;
+            else if (p.col_route == FP4_ROUTE_NVFP4_GLOBAL)
+                senc_col = h16 ? nv_senc(__uint_as_float(ws[1 + (p.R >> 7) + (p.C >> 7)])) : senc_w;
+            else
+                senc_col = nv_senc(__uint_as_float(ws[1 + (p.R >> 7) + tx]));
         }
         if (t == 0) {
-            if (p.route == FP4_ROUTE_NVFP4_LOCAL && !w2d) {
-                if (do_row && tx == 0) p.row_outer[ty] = senc_row;
-                if (do_col && ty == 0) p.col_outer[tx] = senc_col;
-            } else if (tx == 0 && ty == 0) {
-                if (do_row) p.row_outer[0] = senc_row;
-                if (do_col) p.col_outer[0] = senc_col;
+            if (NVR && do_row) {
+                if (p.row_route == FP4_ROUTE_NVFP4_LOCAL && !w2d) {
+                    if (tx == 0) p.row_outer[ty] = senc_row;
+                } else if (tx == 0 && ty == 0) {
+                    p.row_outer[0] = senc_row;
+                }
+            }
+            if (NVC && do_col) {
+                if (p.col_route == FP4_ROUTE_NVFP4_LOCAL && !w2d) {
+                    if (ty == 0) p.col_outer[tx] = senc_col;
+                } else if (tx == 0 && ty == 0) {
+                    p.col_outer[0] = senc_col;
+                }
             }
         }
     }
@@ -277,7 +319,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             s.seg_amax[r * 8 + 2 * j + 1] = max(lane_lo_f32bits(a1), lane_hi_f32bits(a1));
         }
         __syncthreads();
-        if (!NV) {
+        if (!NVR || !NVC) {
             // 16 tiles of 32x32: 16 threads per tile, two rows each
             const int tile = t >> 4, part = t & 15, tr = tile >> 2, tc = tile & 3;
             uint32_t m = 0;
@@ -295,7 +337,8 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 if (__fmul_rn(__uint_as_float(m), exp2_neg(e)) < 5.22f && e > -127) e -= 1;
                 s.tile_e[tile] = e;
             }
-        } else {
+        }
+        if (NVR || NVC) {
             // 64 tiles of 16x16: 4 threads per tile, four rows each
             const int tile = t >> 2, part = t & 3, tr = tile >> 3, tc = tile & 7;
             uint32_t m = 0;
@@ -306,7 +349,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             if (part == 0) {
                 check_finite(m);
                 float mm;
-                s.tile_d[tile] = nv_block_scale(__uint_as_float(m), senc_row, mm);
+                s.tile_d[tile] = nv_block_scale(__uint_as_float(m), senc_w, mm);
                 s.tile_m[tile] = mm;
             }
         }
@@ -328,7 +371,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             }
             float m0, m1;
             if (w2d) {
-                if (!NV) {
+                if (!NVR) {
                     const int e = s.tile_e[(r >> 5) * 4 + j];
                     m0 = m1 = exp2_neg(e);
                     s.row_sc[atom_off(r, j)] = (uint8_t)(e + 127);
@@ -339,7 +382,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                     s.row_sc[atom_off(r, 2 * j)] = (uint8_t)s.tile_d[tl];
                     s.row_sc[atom_off(r, 2 * j + 1)] = (uint8_t)s.tile_d[tl + 1];
                 }
-            } else if (!NV) {
+            } else if (!NVR) {
                 const uint32_t a2 = amax_words<16>(w);
                 segment_scale<false>(max(lane_lo_f32bits(a2), lane_hi_f32bits(a2)), 0, 0.f, s.row_sc, r, j, m0, m1);
             } else {
@@ -368,19 +411,19 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
     //    (2 cp, 2 cp + 1) is read as 32 bf16x2 words down the tile, and each
     //    column is one 32-value segment of its stored row (blocks along the rows)
     if (do_col) {
-        const bool had = (p.flags & FP4_FLAG_HADAMARD_COL) != 0;
+        const bool had = (p.flags & FP4_FLAG_HADAMARD_COL) != 0;  // H32 (MXFP4)
         const int cp = t & 63, j = t >> 6;
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tbuf[(j * 32 + i) * LDS + 2 * cp]);
-        if (had) {
+        if (had || h16) {
             // the sign of position i (mod 16) applies to both columns of the pair
 #pragma unroll
             for (int i = 0; i < 32; ++i) w[i] ^= ((p.sign_mask >> (i & 15)) & 1u) * 0x80008000u;
         }
         uint32_t a_lo0 = 0, a_hi0 = 0, a_lo1 = 0, a_hi1 = 0;  // NV: [h][block]
-        if (!had && !w2d) {
-            if (!NV) {
+        if (!had && !h16 && !w2d) {
+            if (!NVC) {
                 const uint32_t a2 = amax_words<32>(w);
                 a_lo0 = lane_lo_f32bits(a2);
                 a_hi0 = lane_hi_f32bits(a2);
@@ -399,7 +442,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             unpack_lane(w, h, v);
             float m0, m1;
             if (w2d) {
-                if (!NV) {
+                if (!NVC) {
                     const int e = s.tile_e[j * 4 + (c >> 5)];
                     m0 = m1 = exp2_neg(e);
                     s.col_sc[atom_off(c, j)] = (uint8_t)(e + 127);
@@ -412,9 +455,15 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 }
             } else if (had) {
                 hadamard32_nosign(v);
-                segment_scale<NV>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
+                segment_scale<NVC>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
+            } else if (h16) {
+                hadamard16x2_nosign(v);
+                if (NVC)
+                    segment_scale<true>(amax_bits16(v), amax_bits16(v + 16), senc_col, s.col_sc, c, j, m0, m1);
+                else
+                    segment_scale<false>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
             } else {
-                segment_scale<NV>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1);
+                segment_scale<NVC>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1);
             }
             *reinterpret_cast<uint4*>(&s.col_codes[col_stage_off(c, j)]) = pack_rn32(v, m0, m1);
         }
@@ -429,10 +478,10 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             *reinterpret_cast<uint4*>(p.row_codes + (r0 + rr) * (p.C >> 1) + (c0 >> 1) + part * 16) =
                 *reinterpret_cast<const uint4*>(&s.row_codes[rr * 64 + part * 16]);
         }
-        const int nat = NV ? 2 : 1;
+        const int nat = NVR ? 2 : 1;
         if (t < nat * 32) {
-            int64_t atoms_per_rowblock = NV ? (p.C >> 6) : (p.C >> 7);
-            int64_t a0 = (r0 >> 7) * atoms_per_rowblock + (NV ? (c0 >> 6) : (c0 >> 7));
+            int64_t atoms_per_rowblock = NVR ? (p.C >> 6) : (p.C >> 7);
+            int64_t a0 = (r0 >> 7) * atoms_per_rowblock + (NVR ? (c0 >> 6) : (c0 >> 7));
             *reinterpret_cast<uint4*>(p.row_scales + a0 * 512 + t * 16) =
                 *reinterpret_cast<const uint4*>(&s.row_sc[t * 16]);
         }
@@ -444,10 +493,10 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             *reinterpret_cast<uint4*>(p.col_codes + (c0 + cc) * (p.R >> 1) + (r0 >> 1) + part * 16) =
                 *reinterpret_cast<const uint4*>(&s.col_codes[col_stage_off(cc, part)]);
         }
-        const int nat = NV ? 2 : 1;
+        const int nat = NVC ? 2 : 1;
         if (t < nat * 32) {
-            int64_t atoms_per_rowblock = NV ? (p.R >> 6) : (p.R >> 7);
-            int64_t a0 = (c0 >> 7) * atoms_per_rowblock + (NV ? (r0 >> 6) : (r0 >> 7));
+            int64_t atoms_per_rowblock = NVC ? (p.R >> 6) : (p.R >> 7);
+            int64_t a0 = (c0 >> 7) * atoms_per_rowblock + (NVC ? (r0 >> 6) : (r0 >> 7));
             *reinterpret_cast<uint4*>(p.col_scales + a0 * 512 + t * 16) =
                 *reinterpret_cast<const uint4*>(&s.col_sc[t * 16]);
         }
@@ -477,7 +526,7 @@ FP4_DEV void prefetch_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_
 // order) with two tile buffers: while one tile is encoded the next one is
 // already in flight, so its load latency hides behind the encoding.  With an
 // RMSNorm pre-op the tile is loaded (and transformed) synchronously.
-template <bool NV>
+template <bool NVR, bool NVC>
 __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
@@ -501,23 +550,29 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p
             load_tile(p, ty * TILE, tx * TILE, cur, true);
         }
         __syncthreads();
-        encode_tile<NV>(p, s, cur, ty, tx);
+        encode_tile<NVR, NVC>(p, s, cur, ty, tx);
         __syncthreads();  // staging buffers and `cur` are free for the next tile
     }
 }
 
 // Tile-amax pre-pass for NVFP4: max |x| of each 128x128 tile folded into the
 // tensor slot ws[0], the tile's row-strip slot and its column-strip slot.
+// When the column view is NVFP4 through H16, its factors are those of the
+// transformed values: the column-strip slots and the last slot (the global
+// column factor) then take the maxima of the H16 output of each 16-row block.
 __global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
-    __shared__ uint32_t red[THREADS / 32];
+    __shared__ uint32_t red[2][THREADS / 32];
     extern __shared__ __align__(16) uint8_t amax_smem[];
     uint16_t* tile = reinterpret_cast<uint16_t*>(amax_smem);
     uint32_t* ws = p.amax_ws;
-    const int64_t n_row_strips = p.R / TILE;
+    const int64_t n_row_strips = p.R / TILE, n_col_strips = p.C / TILE;
     const int t = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.y * TILE, c0 = (int64_t)blockIdx.x * TILE;
-    uint32_t m = 0;
-    if (p.pre != PRE_NONE) {
+    const bool col_h16 = (p.flags & FP4_FLAG_HADAMARD16_COL) && (p.views & FP4_VIEW_COL) &&
+                         p.col_route != FP4_ROUTE_MXFP4;
+    const bool staged = p.pre != PRE_NONE || col_h16;
+    uint32_t m = 0, mc = 0;
+    if (staged) {
         load_tile(p, r0, c0, tile, false);
         __syncthreads();
     }
@@ -525,8 +580,8 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
     for (int i = 0; i < 8; ++i) {
         int q = t + i * THREADS;
         int rr = q >> 4, cc = (q & 15) * 8;
-        uint4 d = p.pre != PRE_NONE ? *reinterpret_cast<const uint4*>(&tile[rr * LDS + cc])
-                                    : *reinterpret_cast<const uint4*>(p.x + (r0 + rr) * p.ld + c0 + cc);
+        uint4 d = staged ? *reinterpret_cast<const uint4*>(&tile[rr * LDS + cc])
+                         : *reinterpret_cast<const uint4*>(p.x + (r0 + rr) * p.ld + c0 + cc);
         uint32_t w[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
@@ -534,20 +589,49 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
             m = max(m, w[b] & 0x7FFF0000u);
         }
     }
+    if (col_h16) {
+        // (column pair, 16-row block) tasks: signs, H16 down the column, max
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const int task = t + k * THREADS, cp = task & 63, jb = task >> 6;
+            float v[32];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if ((t & 31) == 0) red[t >> 5] = m;
+            for (int i = 0; i < 16; ++i) {
+                uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(jb * 16 + i) * LDS + 2 * cp]);
+                w ^= ((p.sign_mask >> i) & 1u) * 0x80008000u;
+                v[i] = bf16_lo(w);
+                v[16 + i] = bf16_hi(w);
+            }
+            hadamard16x2_nosign(v);
+            mc = max(mc, max(amax_bits16(v), amax_bits16(v + 16)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        mc = max(mc, __shfl_xor_sync(0xFFFFFFFFu, mc, o));
+    }
+    if ((t & 31) == 0) {
+        red[0][t >> 5] = m;
+        red[1][t >> 5] = mc;
+    }
     __syncthreads();
     if (t == 0) {
-        for (int i = 1; i < THREADS / 32; ++i) m = max(m, red[i]);
+        for (int i = 1; i < THREADS / 32; ++i) {
+            m = max(m, red[0][i]);
+            mc = max(mc, red[1][i]);
+        }
         check_finite(m);
         atomicMax(&ws[0], m);
         atomicMax(&ws[1 + blockIdx.y], m);
-        atomicMax(&ws[1 + n_row_strips + blockIdx.x], m);
+        if (col_h16) {
+            atomicMax(&ws[1 + n_row_strips + blockIdx.x], mc);
+            atomicMax(&ws[1 + n_row_strips + n_col_strips], mc);
+        } else {
+            atomicMax(&ws[1 + n_row_strips + blockIdx.x], m);
+        }
     }
 }
-
-}  // namespace
 
 // CTAs of the encoder: two tiles per CTA, so that the second tile's load
 // overlaps the first one's encoding.  (Measured against one tile per CTA and
@@ -556,34 +640,49 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
 // the latency-bound weight and activation producers.)
 unsigned encoder_grid(int64_t n_tiles) { return (unsigned)((n_tiles + 1) / 2); }
 
-int launch_quantize(const QuantParams& p, cudaStream_t stream) {
-    dim3 grid((unsigned)(p.C / TILE), (unsigned)(p.R / TILE));
-    const int64_t n_tiles = (p.C / TILE) * (p.R / TILE);
+template <bool NVR, bool NVC>
+int launch_encoder(const QuantParams& p, cudaStream_t stream) {
     const size_t smem = sizeof(SmemQ);
-    const bool nv = p.route != FP4_ROUTE_MXFP4;
-    if (nv) {
-        size_t ws_bytes = (size_t)(1 + p.R / TILE + p.C / TILE) * 4;
-        if (cudaMemsetAsync(p.amax_ws, 0, ws_bytes, stream) != cudaSuccess) return FP4_ERR_CUDA;
-        const size_t amax_smem = p.pre != PRE_NONE ? sizeof(uint16_t) * TILE * LDS : 0;
+    static bool attr_done = false;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return FP4_ERR_CUDA;
+        cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        attr_done = true;
+    }
+    const int64_t n_tiles = (p.C / TILE) * (p.R / TILE);
+    quantize_tile_kernel<NVR, NVC><<<encoder_grid(n_tiles), THREADS, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t quant_workspace_slots(int64_t R, int64_t C, int row_route, int col_route, unsigned views, unsigned flags) {
+    const bool nv_row = (views & FP4_VIEW_ROW) && row_route != FP4_ROUTE_MXFP4;
+    const bool nv_col = (views & FP4_VIEW_COL) && col_route != FP4_ROUTE_MXFP4;
+    if (!nv_row && !nv_col) return 0;
+    return (size_t)(1 + R / TILE + C / TILE) + ((nv_col && (flags & FP4_FLAG_HADAMARD16_COL)) ? 1 : 0);
+}
+
+int launch_quantize(const QuantParams& p, cudaStream_t stream) {
+    const bool do_row = (p.views & FP4_VIEW_ROW) != 0, do_col = (p.views & FP4_VIEW_COL) != 0;
+    // a view that is not produced takes the other view's format
+    const bool nvr = (do_row ? p.row_route : p.col_route) != FP4_ROUTE_MXFP4;
+    const bool nvc = (do_col ? p.col_route : p.row_route) != FP4_ROUTE_MXFP4;
+    const size_t slots = quant_workspace_slots(p.R, p.C, p.row_route, p.col_route, p.views, p.flags);
+    if (slots) {
+        if (cudaMemsetAsync(p.amax_ws, 0, slots * 4, stream) != cudaSuccess) return FP4_ERR_CUDA;
+        const bool col_h16 = (p.flags & FP4_FLAG_HADAMARD16_COL) && do_col && p.col_route != FP4_ROUTE_MXFP4;
+        const size_t amax_smem = (p.pre != PRE_NONE || col_h16) ? sizeof(uint16_t) * TILE * LDS : 0;
+        dim3 grid((unsigned)(p.C / TILE), (unsigned)(p.R / TILE));
         nv_amax_kernel<<<grid, THREADS, amax_smem, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return FP4_ERR_CUDA;
-        static bool attr_nv = false;
-        if (!attr_nv) {
-            cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-            attr_nv = true;
-        }
-        quantize_tile_kernel<true><<<encoder_grid(n_tiles), THREADS, smem, stream>>>(p);
-    } else {
-        static bool attr_mx = false;
-        if (!attr_mx) {
-            cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-            attr_mx = true;
-        }
-        quantize_tile_kernel<false><<<encoder_grid(n_tiles), THREADS, smem, stream>>>(p);
     }
-    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+    if (nvr && nvc) return launch_encoder<true, true>(p, stream);
+    if (nvr) return launch_encoder<true, false>(p, stream);
+    if (nvc) return launch_encoder<false, true>(p, stream);
+    return launch_encoder<false, false>(p, stream);
 }
 
 int quant_status(cudaStream_t stream, int* code, bool reset) {

@@ -94,8 +94,12 @@ enum fp4_flag {
     FP4_FLAG_WEIGHT_2D = 1,     /* 2D32 (MX, adaptive finer scale when a/s < 0.87) or 2D16 (NV) weight
                                    encoding shared by both views (Sec. 2.4, Eqs. 7-8) */
     FP4_FLAG_SR_ROW = 2,        /* stochastic rounding of the row view (Sec. 2.5, Eq. 9) */
-    FP4_FLAG_HADAMARD_COL = 4   /* fixed-sign H32 on the column view before quantization
+    FP4_FLAG_HADAMARD_COL = 4,  /* fixed-sign H32 on the column view before quantization
                                    (Sec. 2.5, Eq. 10; MXFP4 only) */
+    FP4_FLAG_HADAMARD16_COL = 8 /* fixed-sign H16 on the column view before quantization
+                                   (Sec. 2.5: the NVFP4 Wgrad transform; with every sign
+                                   +1 the plain H16 of the operand-wise hybrid, Sec. 3.3);
+                                   any route */
 };
 
 /* GEMM output element types. */
@@ -126,9 +130,10 @@ FP4_API const char* fp4_status_string(int code);
 FP4_API int fp4_tensor_bytes(int route, int64_t rows, int64_t cols, unsigned flags, size_t* codes_bytes,
                      size_t* scale_bytes, int32_t* outer_count);
 
-/* Workspace bytes fp4_quantize needs for this route and shape (0 for MXFP4;
- * (1 + rows/128 + cols/128) * 4 for NVFP4, the amax slots of the outer-factor
- * pre-pass).  Host only. */
+/* Workspace bytes fp4_quantize needs for this route, shape, views and flags
+ * (0 for MXFP4; (1 + rows/128 + cols/128) * 4 for NVFP4, the amax slots of the
+ * outer-factor pre-pass, plus 4 when the column view is H16-transformed).
+ * Host only. */
 FP4_API int fp4_quantize_workspace_bytes(int route, int64_t rows, int64_t cols, unsigned views, unsigned flags,
                                  size_t* bytes);
 
@@ -144,9 +149,14 @@ FP4_API int fp4_quantize_workspace_bytes(int route, int64_t rows, int64_t cols, 
  *                 word (i%8)/2, low half for even i;
  *                 FP4_FLAG_HADAMARD_COL: H32 = Sylvester H32 x diag(signs
  *                 repeated over both halves) / sqrt(32) on every aligned
- *                 32-value block of the column view (MXFP4 only).
+ *                 32-value block of the column view (MXFP4 only);
+ *                 FP4_FLAG_HADAMARD16_COL: H16 = Sylvester H16 x diag(signs)
+ *                 / 4 on every aligned 16-value block of the column view (any
+ *                 route; an NVFP4 view then takes its outer factors from the
+ *                 transformed values).  The two are exclusive, and neither
+ *                 combines with WEIGHT_2D.
  *  hadamard_signs host array of 16 int8 values, each +1 or -1 (read only when
- *                 FP4_FLAG_HADAMARD_COL is set).
+ *                 a Hadamard flag is set; all +1 gives plain H16).
  *  row_out/col_out caller-filled codes/scales/outer pointers for each requested
  *                 view (may be NULL for a view not requested); the call sets
  *                 rows, cols, route and outer_count.
@@ -159,6 +169,29 @@ FP4_API int fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, 
                  unsigned flags, uint64_t sr_seed, uint64_t sr_offset, const int8_t* hadamard_signs,
                  fp4_tensor* row_out, fp4_tensor* col_out, void* workspace, size_t workspace_bytes,
                  fp4_stream_t stream);
+
+/* The operand-wise hybrid producer ("Format-Aware Fusion for Fast FP4
+ * Pretraining", Sec. 3.3): one read of x emits the row view under row_route
+ * and the column view under col_route.  For the hybrid linear, the gradient
+ * dY takes (NVFP4_LOCAL row view with FP4_FLAG_SR_ROW -> Dgrad, MXFP4 column
+ * view with FP4_FLAG_HADAMARD16_COL (plain, all signs +1) or
+ * FP4_FLAG_HADAMARD_COL -> Wgrad) and the weight W takes (MXFP4 2D32 row view
+ * -> Fprop, NVFP4_LOCAL 2D16 column view under the tensor factor -> Dgrad),
+ * with FP4_FLAG_WEIGHT_2D giving each view its own format's 2D encoding.
+ * Every argument is as for fp4_quantize, with each view's rules taken from
+ * its own route (H32 needs an MXFP4 column view; an NVFP4 view needs an
+ * `outer` array).  fp4_quantize(route) is this call with both routes equal.
+ * workspace: fp4_quantize_hybrid_workspace_bytes() bytes. */
+FP4_API int fp4_quantize_hybrid(const void* x, int64_t rows, int64_t cols, int64_t ld, int row_route, int col_route,
+                                unsigned views, unsigned flags, uint64_t sr_seed, uint64_t sr_offset,
+                                const int8_t* hadamard_signs, fp4_tensor* row_out, fp4_tensor* col_out,
+                                void* workspace, size_t workspace_bytes, fp4_stream_t stream);
+
+/* Workspace bytes of fp4_quantize_hybrid: 4 bytes per amax slot when any
+ * requested view is NVFP4 (1 + rows/128 + cols/128 slots, one more when the
+ * NVFP4 column view is H16-transformed), else 0.  Host only. */
+FP4_API int fp4_quantize_hybrid_workspace_bytes(int row_route, int col_route, int64_t rows, int64_t cols,
+                                                unsigned views, unsigned flags, size_t* bytes);
 
 /* fp4_quantize without a workspace argument, for callers that cannot
  * allocate device memory when they quantize (a runtime whose pool owns all

@@ -91,6 +91,8 @@ def _declare(L):
         "orc_inv_sqrt32_f32": (ctypes.c_float, []),
         "orc_hadamard32_f32": (None, [_f32p, _i8p]),
         "orc_hadamard32_rows": (None, [_f32p, _i64, _i64, _i8p]),
+        "orc_hadamard16_f32": (None, [_f32p, _i8p]),
+        "orc_hadamard16_rows": (None, [_f32p, _i64, _i64, _i8p]),
         "orc_sylvester_h32": (None, [_i8p]),
         "orc_mx_quantize_rows": (None, [_f32p, _i64, _i64, ctypes.c_int, _u64, _u64, _u64, _i64, _u8p, _u8p]),
         "orc_mx_quantize_weight2d": (None, [_f32p, _i64, _i64, _u8p, _u8p]),
@@ -189,6 +191,15 @@ def hadamard32_f32(v, signs) -> np.ndarray:
     return y
 
 
+def hadamard16_f32(v, signs) -> np.ndarray:
+    """Fixed-sign H16 of 16 binary32 values (signs of +-1; all +1 is plain H16)."""
+    y = np.ascontiguousarray(v, dtype=np.float32).copy()
+    s = np.ascontiguousarray(signs, dtype=np.int8)
+    assert y.shape == (16,) and s.shape == (16,)
+    lib().orc_hadamard16_f32(_p(y, _f32p), _p(s, _i8p))
+    return y
+
+
 def sylvester_h32() -> np.ndarray:
     h = np.zeros((32, 32), np.int8)
     lib().orc_sylvester_h32(_p(h, _i8p))
@@ -253,6 +264,7 @@ def _sr_index(origin, cols, C):
 
 def quantize(x_bits: np.ndarray, route: str, view: str, *, sr: bool = False, seed: int = 0,
              offset: int = 0, hadamard: bool = False, signs=None, weight2d: bool = False,
+             hadamard16: bool = False,
              sr_origin: tuple[int, int] = (0, 0), sr_cols: int | None = None) -> dict:
     """Quantize a bf16 tensor (uint16 bits, R x C) into one view.
 
@@ -260,6 +272,10 @@ def quantize(x_bits: np.ndarray, route: str, view: str, *, sr: bool = False, see
     view     'row' (scale blocks along C) | 'col' (blocks along R, stored transposed)
     sr       stochastic rounding; only allowed on the row view (Sec. 2.5)
     hadamard fixed-sign H32 before quantization; only on the MX column view
+    hadamard16
+             fixed-sign H16 (all signs +1: plain H16) on each aligned 16-value
+             block of the column view before quantization, any route; an
+             NVFP4 outer factor is then the transformed tensor's
     weight2d 2D32 (MX) or 2D16 (NV) shared weight encoding (Sec. 2.4)
     sr_origin, sr_cols
              when x is a block of a larger tensor: the (row, column) of its
@@ -274,6 +290,8 @@ def quantize(x_bits: np.ndarray, route: str, view: str, *, sr: bool = False, see
     assert route in ROUTES and view in ("row", "col")
     if sr and view != "row":
         raise ValueError("SR applies to the row-facing view only")
+    if hadamard16 and (view != "col" or hadamard or weight2d):
+        raise ValueError("H16 applies to a column-facing activation or gradient view only")
     if hadamard and (view != "col" or route != "mx"):
         raise ValueError("H32 applies to the MX column-facing view only")
     xf = bf16_to_f32(np.ascontiguousarray(x_bits))
@@ -306,11 +324,16 @@ def quantize(x_bits: np.ndarray, route: str, view: str, *, sr: bool = False, see
         assert s.shape == (16,)
         v = v.copy()
         lib().orc_hadamard32_rows(_p(v, _f32p), v.shape[0], v.shape[1], _p(s, _i8p))
+    if hadamard16:
+        s = np.ascontiguousarray(signs, dtype=np.int8)
+        assert s.shape == (16,)
+        v = v.copy()
+        lib().orc_hadamard16_rows(_p(v, _f32p), v.shape[0], v.shape[1], _p(s, _i8p))
     if route == "mx":
         codes, scales = _mx_rows(v, sr, seed, offset, *_sr_index(sr_origin, sr_cols, C))
         return dict(codes=codes, scales=scales, senc=None, fmt=0, bs=32)
     if route == "nv_global":
-        senc_row = np.full(v.shape[0], nv_senc(amax_f32(xf)), np.float32)
+        senc_row = np.full(v.shape[0], nv_senc(amax_f32(np.ascontiguousarray(v))), np.float32)
     else:
         senc_row = _strip_senc(v)
     codes, scales = _nv_rows(v, senc_row, sr, seed, offset, *_sr_index(sr_origin, sr_cols, C))

@@ -281,6 +281,32 @@ void orc_hadamard32_rows(float* x, int64_t R, int64_t C, const int8_t signs[16])
         for (int64_t b = 0; b < C / 32; ++b) orc_hadamard32_f32(x + r * C + b * 32, signs);
 }
 
+/* Fixed-sign H16 ("Format-Aware Fusion for Fast FP4 Pretraining", Sec. 2.5
+ * and Appendix A.1; the NVFP4 Wgrad transform and, with every sign +1,
+ * the plain H16 of the operand-wise hybrid, Sec. 3.3): R = H16 D / 4 on
+ * 16 binary32 values in place -- the 16 signs applied once, the butterflies
+ * of stride 1, 2, 4 and 8 (a + b, a - b), then the multiply by 1/sqrt(16) =
+ * 0.25 (exact). */
+void orc_hadamard16_f32(float y[16], const int8_t signs[16])
+{
+    for (int i = 0; i < 16; ++i) y[i] = y[i] * (float)signs[i];
+    for (int h = 1; h < 16; h *= 2)
+        for (int j = 0; j < 16; ++j)
+            if ((j & h) == 0) {
+                float a = y[j], b = y[j + h];
+                y[j] = a + b;
+                y[j + h] = a - b;
+            }
+    for (int i = 0; i < 16; ++i) y[i] = y[i] * 0.25f;
+}
+
+/* The same transform on every aligned 16-value block of every row. */
+void orc_hadamard16_rows(float* x, int64_t R, int64_t C, const int8_t signs[16])
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t b = 0; b < C / 16; ++b) orc_hadamard16_f32(x + r * C + b * 16, signs);
+}
+
 /* Explicit Sylvester matrix H_32 (entries +-1): H_1 = [1],
  * H_2n = [[H_n, H_n], [H_n, -H_n]].  Written row-major into h[32*32]. */
 void orc_sylvester_h32(int8_t* h)

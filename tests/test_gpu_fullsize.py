@@ -275,3 +275,38 @@ def test_stack32_hybrid_full_step():
         for name, a, b in (("w2", gv["dF"][1], s["h"][1]), ("w13", gv["da13"][1], s["y2"][1]),
                            ("o", gv["dr2"][1], s["attn"][1]), ("qkv", gv["dqkv"][1], s["y1"][1])):
             assert torch.equal(F.fp4_linear_wgrad(a, b), blk.dw[name]), f"{blk.route} block dW{name}"
+
+
+# ------------------------------------------- operand-wise hybrid, W1 shape ----
+def test_operand_hybrid_w1_full():
+    """MXFP4 Fprop and Wgrad (plain H16 on the pair), CTA-local NVFP4 Dgrad
+    with row SR, at the W1 shape (Sec. 3.3), as the benchmark's hybrid leg
+    runs it."""
+    T, di, do = 8192, 4096, 14336
+    t = config_tensors("c2_mx_w1")
+    ones = [1] * 16
+    X, W, DY = to_dev(t["x"]), to_dev(t["w"]), to_dev(t["dy"])
+    h16 = F.FP4_FLAG_HADAMARD16_COL
+    xr, xc = F.fp4_quantize(X, "mx", 3, h16, hadamard_signs=ones)
+    wr, wc = F.fp4_quantize_hybrid(W, "mx", "nv_local", 3, F.FP4_FLAG_WEIGHT_2D)
+    dr, dc = F.fp4_quantize_hybrid(DY, "nv_local", "mx", 3, F.FP4_FLAG_SR_ROW | h16, sr_seed=4, sr_offset=0,
+                                   hadamard_signs=ones)
+    Y = F.fp4_linear_fprop(xr, wr)
+    DX = F.fp4_linear_dgrad(dr, wc)
+    DW = F.fp4_linear_wgrad(dc, xc)
+    torch.cuda.synchronize()
+    assert F.fp4_status() == F.FP4_OK
+    del X, W, DY
+    s1 = np.ones(16, np.int8)
+    ov = dict(xr=oracle.quantize(t["x"], "mx", "row"),
+              xc=oracle.quantize(t["x"], "mx", "col", hadamard16=True, signs=s1),
+              wr=oracle.quantize(t["w"], "mx", "row", weight2d=True),
+              wc=oracle.quantize(t["w"], "nv_local", "col", weight2d=True),
+              dr=oracle.quantize(t["dy"], "nv_local", "row", sr=True, seed=4, offset=0),
+              dc=oracle.quantize(t["dy"], "mx", "col", hadamard16=True, signs=s1))
+    for k, v in dict(xr=xr, xc=xc, wr=wr, wc=wc, dr=dr, dc=dc).items():
+        same_view(v, ov[k], f"hybrid W1 {k}")
+    rng = np.random.default_rng(12)
+    check_sampled(Y, ov["xr"], ov["wr"], "hybrid Fprop (MX)", rng)
+    check_sampled(DX, ov["dr"], ov["wc"], "hybrid Dgrad (CTA-local)", rng)
+    check_sampled(DW, ov["dc"], ov["xc"], "hybrid Wgrad (MX, H16 pair)", rng)
