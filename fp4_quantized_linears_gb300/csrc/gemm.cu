@@ -351,6 +351,18 @@ FP4_DEV uint32_t mx_block_sr(const float* v, uint64_t g0, uint64_t seed, uint64_
     return (uint32_t)(e + 127);
 }
 
+// Two binary32 values rounded to nearest-even bf16 and packed (lo in the low
+// half), one conversion instruction; the same rounding as f32_to_bf16_rn.
+FP4_DEV uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+FP4_DEV void store_words16(uint16_t* dst, const uint32_t* w) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+}
+
 FP4_DEV void store_bf16x32(uint16_t* dst, const float* v) {
 #pragma unroll
     for (int i = 0; i < 32; i += 8) {
@@ -793,42 +805,59 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else if constexpr (EPI == EPI_SWIGLU_FWD) {
                 // output columns [64*half, 64*half + 64) of this 128-wide tile:
                 // a1 in accumulator columns 0..127, a3 in 128..255
-                uint32_t r1[64], r3[64];
+                uint32_t p1[32], p3[32];  // bf16x2 of the retained a1, a3 (64 columns each)
+                {
+                    uint32_t r1[64], r3[64];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(lane_base + 64 * half + 32 * c, r1 + 32 * c);
-                    tmem_ld32(lane_base + 128 + 64 * half + 32 * c, r3 + 32 * c);
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld32(lane_base + 64 * half + 32 * c, r1 + 32 * c);
+                        tmem_ld32(lane_base + 128 + 64 * half + 32 * c, r3 + 32 * c);
+                    }
+                    tc_fence_before();
+                    if (lane == 0) mbar_arrive(acc_empty);
+                    float alpha = 1.0f;
+                    if (NV)
+                        alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
+                                          __fdiv_rn(1.0f, p.b_outer[0]));
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        p1[i] = bf16x2_rn(__uint_as_float(r1[2 * i]) * alpha, __uint_as_float(r1[2 * i + 1]) * alpha);
+                        p3[i] = bf16x2_rn(__uint_as_float(r3[2 * i]) * alpha, __uint_as_float(r3[2 * i + 1]) * alpha);
+                    }
                 }
-                tc_fence_before();
-                if (lane == 0) mbar_arrive(acc_empty);
                 uint16_t* hs = reinterpret_cast<uint16_t*>(staging);
                 uint8_t* row_atom = staging + BM * ST_LDS * 2;
                 uint8_t* col_atom = row_atom + 512;
-                float alpha = 1.0f;
-                if (NV)
-                    alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
-                                      __fdiv_rn(1.0f, p.b_outer[0]));
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int oc = 64 * half + 32 * c;
                     const int64_t n = n0 + oc;
-                    float h[32], x1[32], x3[32];
+                    store_words16(p.a1 + m * p.f + n, p1 + 16 * c);
+                    store_words16(p.a3 + m * p.f + n, p3 + 16 * c);
+                    float h[32];
+                    uint32_t hp[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        x1[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r1[32 * c + i]) * alpha));
-                        x3[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r3[32 * c + i]) * alpha));
-                        const float s = x1[i] * __frcp_rn(1.0f + __expf(-x1[i]));
-                        h[i] = bf16_to_f32(f32_to_bf16_rn(__fmul_rn(s, x3[i])));
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t w1 = p1[16 * c + i], w3 = p3[16 * c + i];
+                        float hv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float x1 = e ? bf16_hi(w1) : bf16_lo(w1);
+                            const float x3 = e ? bf16_hi(w3) : bf16_lo(w3);
+                            const float sl = x1 * __frcp_rn(1.0f + __expf(-x1));
+                            hv[e] = __fmul_rn(sl, x3);
+                        }
+                        hp[i] = bf16x2_rn(hv[0], hv[1]);
+                        h[2 * i] = bf16_lo(hp[i]);
+                        h[2 * i + 1] = bf16_hi(hp[i]);
                     }
-                    store_bf16x32(p.a1 + m * p.f + n, x1);
-                    store_bf16x32(p.a3 + m * p.f + n, x3);
-                    if (p.tap0) store_bf16x32(p.tap0 + m * p.f + n, h);
+                    if (p.tap0) store_words16(p.tap0 + m * p.f + n, hp);
                     if (p.quantize) {
                         uint4 pk;
                         uint32_t sc = mx_block_rn(h, pk);
                         *reinterpret_cast<uint4*>(p.q_row_codes + m * (p.f >> 1) + (n >> 1)) = pk;
                         row_atom[atom_off(lr, oc >> 5)] = (uint8_t)sc;
-                        store_bf16x32(hs + lr * ST_LDS + oc, h);
+                        store_words16(hs + lr * ST_LDS + oc, hp);
                     }
                 }
                 if (p.quantize) {
@@ -862,52 +891,67 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             } else {
                 // EPI_SWIGLU_BWD: dh for output columns [64*half, 64*half + 64)
-                uint32_t r[64];
+                uint32_t dp[32];  // bf16x2 of dh (64 columns)
+                {
+                    uint32_t r[64];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + 64 * half + 32 * c, r + 32 * c);
-                tc_fence_before();
-                if (lane == 0) mbar_arrive(acc_empty);
+                    for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + 64 * half + 32 * c, r + 32 * c);
+                    tc_fence_before();
+                    if (lane == 0) mbar_arrive(acc_empty);
+                    float alpha = 1.0f;
+                    if (NV)
+                        alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
+                                          __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n0 >> 7)]));
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        dp[i] = bf16x2_rn(__uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
+                }
                 uint16_t* s1 = reinterpret_cast<uint16_t*>(staging);
                 uint16_t* s3 = s1 + BM * ST_LDS;
                 uint8_t* atoms = staging + 2 * BM * ST_LDS * 2;  // row da1, row da3, col da1, col da3
-                float alpha = 1.0f;
-                if (NV)
-                    alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
-                                      __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n0 >> 7)]));
                 const int64_t f2 = 2 * p.f;
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int oc = 64 * half + 32 * c;
                     const int64_t n = n0 + oc;
+                    if (p.tap0) store_words16(p.tap0 + m * p.f + n, dp + 16 * c);
                     float d1[32], d3[32];
-                    {
-                        float dh[32];
+                    uint32_t q1[16], q3[16];
+                    const uint16_t* pa1 = p.a1 + m * p.f + n;
+                    const uint16_t* pa3 = p.a3 + m * p.f + n;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            dh[i] = bf16_to_f32(f32_to_bf16_rn(__uint_as_float(r[32 * c + i]) * alpha));
-                        if (p.tap0) store_bf16x32(p.tap0 + m * p.f + n, dh);
-                        const uint16_t* pa1 = p.a1 + m * p.f + n;
-                        const uint16_t* pa3 = p.a3 + m * p.f + n;
+                    for (int i = 0; i < 32; i += 8) {
+                        const uint4 v1 = *reinterpret_cast<const uint4*>(pa1 + i);
+                        const uint4 v3 = *reinterpret_cast<const uint4*>(pa3 + i);
+                        const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
 #pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            uint4 v1 = *reinterpret_cast<const uint4*>(pa1 + i);
-                            uint4 v3 = *reinterpret_cast<const uint4*>(pa3 + i);
-                            uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t wg = dp[16 * c + i / 2 + j];
+                            float o1[2], o3[2];
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const float x = (j & 1) ? bf16_hi(w1[j >> 1]) : bf16_lo(w1[j >> 1]);
-                                const float y = (j & 1) ? bf16_hi(w3[j >> 1]) : bf16_lo(w3[j >> 1]);
+                            for (int e = 0; e < 2; ++e) {
+                                const float x = e ? bf16_hi(w1[j]) : bf16_lo(w1[j]);
+                                const float y = e ? bf16_hi(w3[j]) : bf16_lo(w3[j]);
+                                const float g = e ? bf16_hi(wg) : bf16_lo(wg);
                                 const float sg = __frcp_rn(1.0f + __expf(-x));
-                                const float g = dh[i + j];
                                 const float dsilu = sg * (1.0f + x * (1.0f - sg));
-                                d1[i + j] = bf16_to_f32(f32_to_bf16_rn(g * y * dsilu));
-                                d3[i + j] = bf16_to_f32(f32_to_bf16_rn(g * (x * sg)));
+                                o1[e] = g * y * dsilu;
+                                o3[e] = g * (x * sg);
                             }
+                            q1[i / 2 + j] = bf16x2_rn(o1[0], o1[1]);
+                            q3[i / 2 + j] = bf16x2_rn(o3[0], o3[1]);
                         }
                     }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        d1[2 * i] = bf16_lo(q1[i]);
+                        d1[2 * i + 1] = bf16_hi(q1[i]);
+                        d3[2 * i] = bf16_lo(q3[i]);
+                        d3[2 * i + 1] = bf16_hi(q3[i]);
+                    }
                     if (p.tap1) {
-                        store_bf16x32(p.tap1 + m * f2 + n, d1);
-                        store_bf16x32(p.tap1 + m * f2 + p.f + n, d3);
+                        store_words16(p.tap1 + m * f2 + n, q1);
+                        store_words16(p.tap1 + m * f2 + p.f + n, q3);
                     }
                     if (p.quantize) {
                         uint4 pk;
@@ -917,8 +961,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         sc = mx_block_sr(d3, (uint64_t)(m * f2 + p.f + n) >> 3, p.seed, p.offset, pk);
                         *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + ((p.f + n) >> 1)) = pk;
                         atoms[512 + atom_off(lr, oc >> 5)] = (uint8_t)sc;
-                        store_bf16x32(s1 + lr * ST_LDS + oc, d1);
-                        store_bf16x32(s3 + lr * ST_LDS + oc, d3);
+                        store_words16(s1 + lr * ST_LDS + oc, q1);
+                        store_words16(s3 + lr * ST_LDS + oc, q3);
                     }
                 }
                 if (p.quantize) {
