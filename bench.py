@@ -484,9 +484,11 @@ def run_legs(args, peaks, only=None) -> dict:
     del X3, t3
     torch.cuda.empty_cache()
 
-    if only not in (None, "swiglu"):
+    if only not in (None, "swiglu", "stack"):
         return out
     # fused SwiGLU FFN, MXFP4, T 16384, d 4096, f 14336
+    if only == "stack":
+        return run_stack_leg(args, out)
     t4 = config_tensors("c4_swiglu", scale_T=args.tokens)
     X4, W13, W2, DY2 = dev(t4["x"]), dev(t4["w13"]), dev(t4["w2"]), dev(t4["dy2"])
     del t4
@@ -529,20 +531,30 @@ def run_legs(args, peaks, only=None) -> dict:
     del X4, W13, W2, DY2, xr, xc, w13r, w13c, w2r, w2c, dyr, dyc, a1, a3, hr, hc, dar, dac, Y2, DX4, DW13, DW2
     torch.cuda.empty_cache()
 
-    # 32-block depth hybrid (blocks 1-27 CTA-local NVFP4, 28-32 MXFP4), T 8192
     if not args.no_stack and only is None:
-        sh = BlockShape()
-        st = FP4LinearStack(32, 27, sh, seed=5)
-        g = torch.Generator(device="cuda").manual_seed(5)
-        x5 = torch.randn((sh.T, sh.d), generator=g, device="cuda").to(torch.bfloat16)
-        dy5 = (torch.randn((sh.T, sh.d), generator=g, device="cuda") * 1e-4).to(torch.bfloat16)
-        ms = _timed(lambda: st.step(x5, dy5, sr_seed=5), 2, 1)
-        fl5 = linear_flops_per_token(sh) * 32 * sh.T
-        out["stack32_hybrid_27nv_5mx_T8192"] = {
-            "ms_per_step": round(ms, 2), "tokens_per_s": round(sh.T / ms * 1e3, 1),
-            "linear_TFLOP/s": round(fl5 / ms / 1e9, 1), "linear_tflop_per_step": round(fl5 / 1e12, 2)}
-        del st, x5, dy5
-        torch.cuda.empty_cache()
+        run_stack_leg(args, out)
+    return out
+
+
+def run_stack_leg(args, out: dict) -> dict:
+    """The depth-hybrid block stack at T 8192 (blocks 1-27 CTA-local NVFP4,
+    28-32 MXFP4); --stack-blocks keeps the same 27/32 split on fewer blocks."""
+    import torch
+    from fp4_quantized_linears_gb300.stack import BlockShape, FP4LinearStack, linear_flops_per_token
+    nb = args.stack_blocks
+    local = (27 * nb) // 32 if nb != 32 else 27
+    sh = BlockShape()
+    st = FP4LinearStack(nb, local, sh, seed=5)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x5 = torch.randn((sh.T, sh.d), generator=g, device="cuda").to(torch.bfloat16)
+    dy5 = (torch.randn((sh.T, sh.d), generator=g, device="cuda") * 1e-4).to(torch.bfloat16)
+    ms = _timed(lambda: st.step(x5, dy5, sr_seed=5), 2, 1)
+    fl5 = linear_flops_per_token(sh) * nb * sh.T
+    out[f"stack{nb}_hybrid_{local}nv_{nb - local}mx_T8192"] = {
+        "ms_per_step": round(ms, 2), "tokens_per_s": round(sh.T / ms * 1e3, 1),
+        "linear_TFLOP/s": round(fl5 / ms / 1e9, 1), "linear_tflop_per_step": round(fl5 / 1e12, 2)}
+    del st, x5, dy5
+    torch.cuda.empty_cache()
     return out
 
 
@@ -638,7 +650,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-legs", action="store_true", help="only the main workload")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-block stack leg")
-    ap.add_argument("--only", choices=["nvfp4", "swiglu"], default=None,
+    ap.add_argument("--stack-blocks", type=int, default=32, help="blocks of the stack leg (profiling-sized runs)")
+    ap.add_argument("--only", choices=["nvfp4", "swiglu", "stack"], default=None,
                     help="run just one of the other legs (sized by --tokens) and print its numbers")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count (default 8192); smaller values make a profiling-sized case")
