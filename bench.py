@@ -484,6 +484,20 @@ def run_legs(args, peaks, only=None) -> dict:
     del X3, t3
     torch.cuda.empty_cache()
 
+    if only in (None, "diagnostic"):
+        # the Dgrad-error diagnostic: E_MX / E_localCTA over 32 blocks x 3
+        # batches of 2048 tokens x 4 components (an accuracy figure, not a rate)
+        from fp4_quantized_linears_gb300.diagnostic import dgrad_diagnostic
+        t0 = time.time()
+        d = dgrad_diagnostic(blocks=32, batches=3, T=2048)
+        out["dgrad_error_diagnostic"] = {
+            "pairs": d["pairs"], "geomean_EMX_over_ElocalCTA": round(d["geomean"], 4),
+            "pairs_lower_for_localCTA": d["favour_local"],
+            "per_component": {k: round(v, 4) for k, v in d["per_component"].items()},
+            "pages_value_on_captured_tensors": 1.292, "wall_s": round(time.time() - t0, 1)}
+        torch.cuda.empty_cache()
+        if only == "diagnostic":
+            return out
     if only not in (None, "swiglu", "stack"):
         return out
     # fused SwiGLU FFN, MXFP4, T 16384, d 4096, f 14336
@@ -651,7 +665,7 @@ def main():
     ap.add_argument("--no-legs", action="store_true", help="only the main workload")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-block stack leg")
     ap.add_argument("--stack-blocks", type=int, default=32, help="blocks of the stack leg (profiling-sized runs)")
-    ap.add_argument("--only", choices=["nvfp4", "swiglu", "stack"], default=None,
+    ap.add_argument("--only", choices=["nvfp4", "swiglu", "stack", "diagnostic"], default=None,
                     help="run just one of the other legs (sized by --tokens) and print its numbers")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count (default 8192); smaller values make a profiling-sized case")
