@@ -484,6 +484,10 @@ def run_legs(args, peaks, only=None) -> dict:
     del X3, t3
     torch.cuda.empty_cache()
 
+    if only in (None, "qkv"):
+        out["qkv_rope_T8192"] = run_qkv_rope_leg()
+        if only == "qkv":
+            return out
     if only in (None, "diagnostic"):
         # the Dgrad-error diagnostic: E_MX / E_localCTA over 32 blocks x 3
         # batches of 2048 tokens x 4 components (an accuracy figure, not a rate)
@@ -548,6 +552,45 @@ def run_legs(args, peaks, only=None) -> dict:
     if not args.no_stack and only is None:
         run_stack_leg(args, out)
     return out
+
+
+def run_qkv_rope_leg(T: int = 8192, d: int = 4096, hq: int = 32, hkv: int = 8, S: int = 4096,
+                     route: str = "nv_local") -> dict:
+    """The QKV boundary with RoPE at Llama-3-8B shapes: the fused projection +
+    RoPE + head-major layout against the plain projection, and the fused
+    backward producer (inverse layout and RoPE + quantization of dQKV) against
+    quantizing an already-assembled dQKV."""
+    import torch
+    import fp4_quantized_linears_gb300 as F
+    N = (hq + 2 * hkv) * 128
+    g = torch.Generator(device="cuda").manual_seed(7)
+    X = torch.randn((T, d), generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn((N, d), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    xr, _ = F.fp4_quantize(X, route, F.FP4_VIEW_ROW)
+    wr, _ = F.fp4_quantize(W, route, F.FP4_VIEW_ROW, F.FP4_FLAG_WEIGHT_2D)
+    pos = torch.arange(S, device="cuda", dtype=torch.float64)[:, None]
+    inv = torch.tensor(500000.0, dtype=torch.float64) ** (-torch.arange(64, dtype=torch.float64) / 64.0)
+    ang = pos * inv.cuda()[None, :]
+    cs, sn = torch.cos(ang).float().contiguous(), torch.sin(ang).float().contiguous()
+    q = torch.empty((hq, T, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((hkv, T, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    Y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    fwd = _timed(lambda: F.fp4_qkv_rope_fwd(xr, wr, cs, sn, S, hq, hkv, q, k, v), 10, 3)
+    plain = _timed(lambda: F.fp4_linear_fprop(xr, wr, Y, F.FP4_OUT_BF16), 10, 3)
+    dq, dk, dv = (t.mul(1e-3) for t in (q, k, v))
+    rv, cv = F.alloc_view(route, T, N, F.FP4_FLAG_SR_ROW), F.alloc_view(route, N, T)
+    ws = torch.empty(max(F.fp4_quantize_workspace_bytes(route, T, N), 16), dtype=torch.uint8, device="cuda")
+    bwd = _timed(lambda: F.fp4_qkv_rope_bwd(dq, dk, dv, cs, sn, S, route, 3, True, 8, 0, None, rv, cv, ws), 10, 3)
+    dY = Y.mul(1e-3)
+    qplain = _timed(lambda: F.fp4_quantize(dY, route, 3, F.FP4_FLAG_SR_ROW, sr_seed=8, row_out=rv, col_out=cv,
+                                           workspace=ws), 10, 3)
+    if F.fp4_status() != F.FP4_OK:
+        raise RuntimeError("device status set in the QKV leg")
+    fl = 2.0 * T * N * d
+    return {"route": route, "fused_fwd_ms": round(fwd, 4), "fused_fwd_TFLOP/s": round(fl / fwd / 1e9, 1),
+            "plain_fprop_ms": round(plain, 4), "fused_bwd_producer_ms": round(bwd, 4),
+            "plain_quantize_ms": round(qplain, 4)}
 
 
 def run_stack_leg(args, out: dict) -> dict:
@@ -665,7 +708,7 @@ def main():
     ap.add_argument("--no-legs", action="store_true", help="only the main workload")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-block stack leg")
     ap.add_argument("--stack-blocks", type=int, default=32, help="blocks of the stack leg (profiling-sized runs)")
-    ap.add_argument("--only", choices=["nvfp4", "swiglu", "stack", "diagnostic"], default=None,
+    ap.add_argument("--only", choices=["nvfp4", "swiglu", "stack", "diagnostic", "qkv"], default=None,
                     help="run just one of the other legs (sized by --tokens) and print its numbers")
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count (default 8192); smaller values make a profiling-sized case")

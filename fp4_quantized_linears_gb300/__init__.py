@@ -114,6 +114,9 @@ def _declare(L):
         "fp4_rmsnorm_bwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int, c_i64, c_i64, ctypes.POINTER(c_sz)]),
         "fp4_swiglu_fwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, tp, tp, vp, vp]),
         "fp4_swiglu_bwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, c_u64, c_u64, tp, tp, vp, vp, vp]),
+        "fp4_qkv_rope_fwd": (ctypes.c_int, [tp, tp, vp, vp, c_i64, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]),
+        "fp4_qkv_rope_bwd": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint, ctypes.c_int, vp, vp, vp, vp, vp, c_i64, c_i64,
+                                            ctypes.c_int, ctypes.c_int, c_u64, c_u64, vp, tp, tp, vp, c_sz, vp]),
         "fp4_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_int)]),
         "fp4_status_reset": (ctypes.c_int, [vp]),
     }
@@ -414,6 +417,49 @@ def fp4_swiglu_bwd(dy2_row: QView, w2_col: QView, f: int, a1: torch.Tensor, a3: 
         _sync_fields(da13_row, rs)
         _sync_fields(da13_col, cs)
     return da13_row, da13_col
+
+
+def fp4_qkv_rope_fwd(x_row: QView, wqkv_row: QView, rope_cos: torch.Tensor, rope_sin: torch.Tensor, seq_len: int,
+                     heads_q: int, heads_kv: int, q=None, k=None, v=None, stream=None):
+    """QKV projection with RoPE into head-major bf16 q [hq][T][128], k, v
+    [hkv][T][128] (rope_cos / rope_sin: float32 CUDA [seq_len][64]).
+    Returns (q, k, v)."""
+    T = x_row.rows
+    dev = x_row.codes.device
+    q = torch.empty((heads_q, T, 128), dtype=torch.bfloat16, device=dev) if q is None else q
+    k = torch.empty((heads_kv, T, 128), dtype=torch.bfloat16, device=dev) if k is None else k
+    v = torch.empty((heads_kv, T, 128), dtype=torch.bfloat16, device=dev) if v is None else v
+    a, b = x_row.struct(), wqkv_row.struct()
+    _check(load().fp4_qkv_rope_fwd(ctypes.byref(a), ctypes.byref(b), _ptr(rope_cos), _ptr(rope_sin), seq_len, heads_q,
+                                   heads_kv, _ptr(q), _ptr(k), _ptr(v), _stream(stream)), "fp4_qkv_rope_fwd")
+    return q, k, v
+
+
+def fp4_qkv_rope_bwd(dq: torch.Tensor, dk: torch.Tensor, dv: torch.Tensor, rope_cos: torch.Tensor,
+                     rope_sin: torch.Tensor, seq_len: int, route, views: int = 3, sr: bool = True, sr_seed: int = 0,
+                     sr_offset: int = 0, dqkv_tap=None, dqkv_row=None, dqkv_col=None, workspace=None, stream=None):
+    """Head-major gradients of the turned Q, K and of V -> the QKV-layout
+    gradient (dQ, dK turned back) quantized into its views.  Returns (row, col)."""
+    rt = _route(route)
+    heads_q, T, _ = dq.shape
+    heads_kv = dk.shape[0]
+    C = (heads_q + 2 * heads_kv) * 128
+    dev = dq.device
+    flags = FP4_FLAG_SR_ROW if sr else 0
+    dqkv_row, dqkv_col = _views(rt, T, C, views, flags, dev, dqkv_row, dqkv_col)
+    need = fp4_quantize_workspace_bytes(rt, T, C, views, 0)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    rs = dqkv_row.struct() if dqkv_row is not None else None
+    cs = dqkv_col.struct() if dqkv_col is not None else None
+    _check(load().fp4_qkv_rope_bwd(rt, views, 1 if sr else 0, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(rope_cos),
+                                   _ptr(rope_sin), T, seq_len, heads_q, heads_kv, sr_seed, sr_offset, _ptr(dqkv_tap),
+                                   ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None,
+                                   _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                                   _stream(stream)), "fp4_qkv_rope_bwd")
+    _sync_fields(dqkv_row, rs)
+    _sync_fields(dqkv_col, cs)
+    return dqkv_row, dqkv_col
 
 
 def fp4_status(stream=None) -> int:

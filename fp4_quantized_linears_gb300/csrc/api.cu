@@ -300,6 +300,62 @@ static int check_operand(const fp4_tensor* t) {
     return FP4_OK;
 }
 
+int fp4_qkv_rope_fwd(const fp4_tensor* x_row, const fp4_tensor* wqkv_row, const float* rope_cos,
+                     const float* rope_sin, int64_t seq_len, int heads_q, int heads_kv, void* q, void* k, void* v,
+                     fp4_stream_t stream) {
+    int rc;
+    if ((rc = check_operand(x_row)) != FP4_OK || (rc = check_operand(wqkv_row)) != FP4_OK) return rc;
+    if (x_row->route != wqkv_row->route) return FP4_ERR_ROUTE_MISMATCH;
+    if (heads_q <= 0 || heads_kv <= 0 || seq_len <= 0) return FP4_ERR_INVALID_ARG;
+    const int64_t T = x_row->rows, d = x_row->cols, N = (int64_t)(heads_q + 2 * heads_kv) * 128;
+    if (wqkv_row->rows != N || wqkv_row->cols != d) return FP4_ERR_UNSUPPORTED_SHAPE;
+    if (T <= 0 || T % 128 || N % 256 || d % 256) return FP4_ERR_UNSUPPORTED_SHAPE;
+    if (!q || !k || !v || !rope_cos || !rope_sin || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(rope_cos) || !aligned16(rope_sin))
+        return FP4_ERR_INVALID_ARG;
+    GemmParams g{};
+    fill_operands(g, x_row, wqkv_row);
+    g.M = T;
+    g.N = N;
+    g.K = d;
+    g.epi = 3;
+    g.q_out = static_cast<uint16_t*>(q);
+    g.k_out = static_cast<uint16_t*>(k);
+    g.v_out = static_cast<uint16_t*>(v);
+    g.rope_cos = rope_cos;
+    g.rope_sin = rope_sin;
+    g.seq_len = seq_len;
+    g.heads_q = heads_q;
+    g.heads_kv = heads_kv;
+    return launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp4_qkv_rope_bwd(int route, unsigned views, int sr, const void* dq, const void* dk, const void* dv,
+                     const float* rope_cos, const float* rope_sin, int64_t rows, int64_t seq_len, int heads_q,
+                     int heads_kv, uint64_t sr_seed, uint64_t sr_offset, void* dqkv_tap, fp4_tensor* dqkv_row,
+                     fp4_tensor* dqkv_col, void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
+    if (heads_q <= 0 || heads_kv <= 0 || seq_len <= 0) return FP4_ERR_INVALID_ARG;
+    const int64_t cols = (int64_t)(heads_q + 2 * heads_kv) * 128;
+    QuantParams p;
+    int rc = prepare_quant(nullptr, true, rows, cols, cols, route, route, views, sr ? FP4_FLAG_SR_ROW : 0, sr_seed,
+                           sr_offset, nullptr, dqkv_row, dqkv_col, workspace, workspace_bytes, &p);
+    if (rc != FP4_OK || rows == 0) return rc;
+    if (!dq || !dk || !dv || !rope_cos || !rope_sin || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(rope_cos) || !aligned16(rope_sin) || (dqkv_tap && !aligned16(dqkv_tap)))
+        return FP4_ERR_INVALID_ARG;
+    p.pre = PRE_ROPE_BWD;
+    p.rope_src[0] = static_cast<const uint16_t*>(dq);
+    p.rope_src[1] = static_cast<const uint16_t*>(dk);
+    p.rope_src[2] = static_cast<const uint16_t*>(dv);
+    p.rope_cos = rope_cos;
+    p.rope_sin = rope_sin;
+    p.seq_len = seq_len;
+    p.heads_q = heads_q;
+    p.heads_kv = heads_kv;
+    p.tap = static_cast<uint16_t*>(dqkv_tap);
+    return launch_quantize(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f, void* a1, void* a3,
                    fp4_tensor* h_row, fp4_tensor* h_col, void* h_tap, fp4_stream_t stream) {
     int rc;

@@ -375,7 +375,7 @@ FP4_DEV void store_bf16x32(uint16_t* dst, const float* v) {
 }
 
 // ----------------------------------------------------------------- kernel -
-enum { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
+enum { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_QKV_ROPE = 3 };
 
 struct KParams {
     const uint8_t* a_scales;
@@ -399,6 +399,14 @@ struct KParams {
     uint8_t* q_col_codes;  // fwd: Q_c(h) [f][M];   bwd: Q_c(da13) [2f][M]
     uint8_t* q_col_scales;
     uint64_t seed, offset;
+    // QKV producer with RoPE: head-major bf16 outputs [heads][M][128]
+    uint16_t* q_out;
+    uint16_t* k_out;
+    uint16_t* v_out;
+    const float* rope_cos;  // [seq_len][64]
+    const float* rope_sin;
+    int64_t seq_len;
+    int heads_q, heads_kv;
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -430,7 +438,9 @@ struct Cfg {
     static constexpr int OUT_BUFS =
         EPI != EPI_STORE ? 0 : (fit(EPI_WARPS * 2 * 4096) >= fit(EPI_WARPS * 4096) ? 2 : 1);
     static constexpr int STAGING =
-        EPI == EPI_STORE ? EPI_WARPS * OUT_BUFS * 4096 : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
+        EPI == EPI_STORE      ? EPI_WARPS * OUT_BUFS * 4096
+        : EPI == EPI_QKV_ROPE ? 0
+                              : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
     static constexpr int STAGES = fit(STAGING);
     static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + RESERVED;
     static_assert(STAGES >= 3, "pipeline depth");
@@ -802,6 +812,67 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
+            } else if constexpr (EPI == EPI_QKV_ROPE) {
+                // this thread's 128 columns are exactly one head of token m:
+                // bf16(acc), RoPE on Q and K heads (rotate-half pairs (i, i+64),
+                // binary32 products and sums, then bf16), head-major store
+                uint32_t pk[64];  // bf16x2 of the head's 128 values
+                {
+                    uint32_t r[128];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + 128 * half + 32 * c, r + 32 * c);
+                    tc_fence_before();
+                    if (lane == 0) mbar_arrive(acc_empty);
+                    float alpha = 1.0f;
+                    if (NV)
+                        alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
+                                          __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : ((n0 >> 7) + half)]));
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        pk[i] = bf16x2_rn(__uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
+                }
+                const int head = (int)((n0 >> 7) + half);
+                const int hqk = p.heads_q + p.heads_kv;
+                uint16_t* dst;
+                if (head < p.heads_q)
+                    dst = p.q_out + ((int64_t)head * p.M + m) * 128;
+                else if (head < hqk)
+                    dst = p.k_out + ((int64_t)(head - p.heads_q) * p.M + m) * 128;
+                else
+                    dst = p.v_out + ((int64_t)(head - hqk) * p.M + m) * 128;
+                if (head < hqk) {
+                    const int64_t pos = m % p.seq_len;
+                    const float4* cp = reinterpret_cast<const float4*>(p.rope_cos + pos * 64);
+                    const float4* sp = reinterpret_cast<const float4*>(p.rope_sin + pos * 64);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {  // pairs i = 8g .. 8g+7
+                        const float4 c0 = cp[2 * g], c1 = cp[2 * g + 1], s0 = sp[2 * g], s1 = sp[2 * g + 1];
+                        const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                        uint32_t lo[4], hi[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t wa = pk[4 * g + j], wb = pk[32 + 4 * g + j];
+                            float l[2], h[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float a = e ? bf16_hi(wa) : bf16_lo(wa);
+                                const float b = e ? bf16_hi(wb) : bf16_lo(wb);
+                                const float c = cv[2 * j + e], sn = sv[2 * j + e];
+                                l[e] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+                                h[e] = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
+                            }
+                            lo[j] = bf16x2_rn(l[0], l[1]);
+                            hi[j] = bf16x2_rn(h[0], h[1]);
+                        }
+                        *reinterpret_cast<uint4*>(dst + 8 * g) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        *reinterpret_cast<uint4*>(dst + 64 + 8 * g) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; i += 4)
+                        *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+                }
             } else if constexpr (EPI == EPI_SWIGLU_FWD) {
                 // output columns [64*half, 64*half + 64) of this 128-wide tile:
                 // a1 in accumulator columns 0..127, a3 in 128..255
@@ -1161,6 +1232,14 @@ KParams kparams_of(const GemmParams& g) {
     p.q_col_scales = g.q_col_scales;
     p.seed = g.seed;
     p.offset = g.offset;
+    p.q_out = g.q_out;
+    p.k_out = g.k_out;
+    p.v_out = g.v_out;
+    p.rope_cos = g.rope_cos;
+    p.rope_sin = g.rope_sin;
+    p.seq_len = g.seq_len;
+    p.heads_q = g.heads_q;
+    p.heads_kv = g.heads_kv;
     return p;
 }
 
@@ -1180,6 +1259,13 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
                     : launch_t<false, 256, EPI_SWIGLU_FWD, 1>(g, kp, units_1, stream);
     }
     g.b_rows = g.N;
+    if (g.epi == 3) {  // QKV projection with RoPE into head-major outputs
+        const int64_t units_1 = (g.M / BM) * (g.N / 256);
+        if (g.nv) return pair ? launch_t<true, 256, EPI_QKV_ROPE, 2>(g, kp, units_1 / 2, stream)
+                              : launch_t<true, 256, EPI_QKV_ROPE, 1>(g, kp, units_1, stream);
+        return pair ? launch_t<false, 256, EPI_QKV_ROPE, 2>(g, kp, units_1 / 2, stream)
+                    : launch_t<false, 256, EPI_QKV_ROPE, 1>(g, kp, units_1, stream);
+    }
     if (g.epi == 2) {  // SwiGLU backward: W2 Dgrad, output [M][f]
         const int64_t units_1 = (g.M / BM) * (g.N / 128);
         if (g.nv) return pair ? launch_t<true, 128, EPI_SWIGLU_BWD, 2>(g, kp, units_1 / 2, stream)

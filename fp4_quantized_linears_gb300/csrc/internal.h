@@ -36,9 +36,17 @@ struct QuantParams {
     const uint16_t* rp;    // r' (bwd)
     const uint16_t* dres;  // incoming residual gradient (bwd), may be NULL
     uint16_t* tap;         // bf16 [R][C] copy of the values quantized (NULL: not written)
+    //   PRE_ROPE_BWD     x = (dq, dk, dv) head-major [heads][R][128]; value = the
+    //                    QKV-layout gradient [R][C], dq and dk turned back
+    //                    (bf16(fl32(fl32(a c) + fl32(b s))), bf16(fl32(fl32(b c) - fl32(a s))))
+    const uint16_t* rope_src[3];
+    const float* rope_cos;  // [seq_len][64]
+    const float* rope_sin;
+    int64_t seq_len;
+    int heads_q, heads_kv;
 };
 
-enum { PRE_NONE = 0, PRE_RMSNORM_FWD = 1, PRE_RMSNORM_BWD = 2 };
+enum { PRE_NONE = 0, PRE_RMSNORM_FWD = 1, PRE_RMSNORM_BWD = 2, PRE_ROPE_BWD = 3 };
 
 int launch_rmsnorm_fwd_stats(const uint16_t* r, const uint16_t* b, int64_t R, int64_t C, int64_t ld, float eps,
                              uint16_t* r_out, float* rstd, cudaStream_t stream);
@@ -79,6 +87,14 @@ struct GemmParams {
     uint8_t* q_col_codes;
     uint8_t* q_col_scales;
     uint64_t seed, offset;
+    // epi 3: the QKV projection with RoPE -> head-major bf16 [heads][M][128]
+    uint16_t* q_out;
+    uint16_t* k_out;
+    uint16_t* v_out;
+    const float* rope_cos;  // [seq_len][64] binary32
+    const float* rope_sin;
+    int64_t seq_len;
+    int heads_q, heads_kv;
 };
 
 int launch_gemm(const GemmParams& p, cudaStream_t stream);

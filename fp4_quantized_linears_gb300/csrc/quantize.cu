@@ -179,6 +179,50 @@ FP4_DEV void load_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* t
         }
         return;
     }
+    if (p.pre == PRE_ROPE_BWD) {
+        // the tile's 128 columns are one head (c0 / 128); each thread takes
+        // 8 values of the low half and their rotate-half partners
+        const int head = (int)(c0 >> 7), hqk = p.heads_q + p.heads_kv;
+        const uint16_t* src = head < p.heads_q ? p.rope_src[0] + (int64_t)head * p.R * 128
+                              : head < hqk     ? p.rope_src[1] + (int64_t)(head - p.heads_q) * p.R * 128
+                                               : p.rope_src[2] + (int64_t)(head - hqk) * p.R * 128;
+#pragma unroll 2
+        for (int i = 0; i < 4; ++i) {
+            const int q = t + i * THREADS, rr = q >> 3, g = q & 7;
+            const int64_t tok = r0 + rr;
+            uint4 lo = *reinterpret_cast<const uint4*>(src + tok * 128 + 8 * g);
+            uint4 hi = *reinterpret_cast<const uint4*>(src + tok * 128 + 64 + 8 * g);
+            if (head < hqk) {
+                const int64_t pos = tok % p.seq_len;
+                const float* cs = p.rope_cos + pos * 64 + 8 * g;
+                const float* sn = p.rope_sin + pos * 64 + 8 * g;
+                uint32_t la[4] = {lo.x, lo.y, lo.z, lo.w}, ha[4] = {hi.x, hi.y, hi.z, hi.w}, lo_o[4], hi_o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float l[2], h[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float a = e ? bf16_hi(la[j]) : bf16_lo(la[j]);
+                        const float b = e ? bf16_hi(ha[j]) : bf16_lo(ha[j]);
+                        const float c = cs[2 * j + e], sv = sn[2 * j + e];
+                        l[e] = __fadd_rn(__fmul_rn(a, c), __fmul_rn(b, sv));
+                        h[e] = __fsub_rn(__fmul_rn(b, c), __fmul_rn(a, sv));
+                    }
+                    lo_o[j] = (uint32_t)f32_to_bf16_rn(l[0]) | ((uint32_t)f32_to_bf16_rn(l[1]) << 16);
+                    hi_o[j] = (uint32_t)f32_to_bf16_rn(h[0]) | ((uint32_t)f32_to_bf16_rn(h[1]) << 16);
+                }
+                lo = make_uint4(lo_o[0], lo_o[1], lo_o[2], lo_o[3]);
+                hi = make_uint4(hi_o[0], hi_o[1], hi_o[2], hi_o[3]);
+            }
+            if (write_tap && p.tap) {
+                *reinterpret_cast<uint4*>(p.tap + tok * p.C + c0 + 8 * g) = lo;
+                *reinterpret_cast<uint4*>(p.tap + tok * p.C + c0 + 64 + 8 * g) = hi;
+            }
+            *reinterpret_cast<uint4*>(&tile[rr * LDS + 8 * g]) = lo;
+            *reinterpret_cast<uint4*>(&tile[rr * LDS + 64 + 8 * g]) = hi;
+        }
+        return;
+    }
 #pragma unroll 2
     for (int i = 0; i < 8; ++i) {
         int q = t + i * THREADS;

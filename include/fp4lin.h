@@ -4,8 +4,9 @@
  * sm_103a (GB300).
  *
  * Two halves, as in the paper's boundary contract (Sec. 3.1):
- *   producers  fp4_quantize, fp4_swiglu_fwd/bwd, fp4_residual_rmsnorm_fwd/bwd
- *              turn BF16 tensors into E2M1 codes plus scales in the physical
+ *   producers  fp4_quantize(_hybrid), fp4_swiglu_fwd/bwd, fp4_residual_rmsnorm_fwd/bwd,
+ *              fp4_qkv_rope_fwd/bwd turn BF16 tensors into E2M1 codes plus
+ *              scales (or the BF16 attention inputs) in the physical
  *              layout the next contraction consumes;
  *   consumers  fp4_linear_fprop/dgrad/wgrad, block-scaled tcgen05 GEMMs.
  *
@@ -230,6 +231,46 @@ FP4_API int fp4_linear_dgrad(const fp4_tensor* dy_row, const fp4_tensor* w_col, 
                      fp4_stream_t stream);
 FP4_API int fp4_linear_wgrad(const fp4_tensor* dy_col, const fp4_tensor* x_col, float* dw, float beta,
                      fp4_stream_t stream);
+
+/* QKV producer with RoPE ("Format-Aware Fusion for Fast FP4 Pretraining",
+ * Sec. 3.2: the Q/K projection applies RoPE and the layout attention
+ * consumes).  One contraction qkv = bf16(X Wqkv^T) (x_row: Q_r(X) [T][d];
+ * wqkv_row: Q_r(Wqkv) [(heads_q + 2 heads_kv) * 128][d], same route) whose
+ * epilogue writes head-major bf16
+ *   q [heads_q][T][128], k [heads_kv][T][128]  turned by RoPE,
+ *   v [heads_kv][T][128]                       copied,
+ * with the QKV columns laid out [Q heads | K heads | V heads] and heads of
+ * 128 values.  RoPE (the rotate-half pairs (i, i + 64) of each head, token t
+ * at position p = t mod seq_len): with c = rope_cos[p][i], s = rope_sin[p][i]
+ * (device binary32 tables [seq_len][64], e.g. cos/sin of p theta^(-i/64)),
+ *   y_i = bf16(fl32(fl32(x_i c) - fl32(x_{i+64} s))),
+ *   y_{i+64} = bf16(fl32(fl32(x_{i+64} c) + fl32(x_i s))).
+ * T a multiple of 128, (heads_q + 2 heads_kv) * 128 a multiple of 256, d a
+ * multiple of 256; q, k, v, tables 16-byte aligned.  Errors as
+ * fp4_linear_fprop, FP4_ERR_UNSUPPORTED_SHAPE for other shapes. */
+FP4_API int fp4_qkv_rope_fwd(const fp4_tensor* x_row, const fp4_tensor* wqkv_row, const float* rope_cos,
+                             const float* rope_sin, int64_t seq_len, int heads_q, int heads_kv, void* q, void* k,
+                             void* v, fp4_stream_t stream);
+
+/* The matching backward producer (Sec. 3.2: inverse layout and RoPE combined
+ * with the QKV gradient production).  From the head-major gradients dq, dk,
+ * dv (device bf16, layouts as the forward's outputs) it forms the QKV-layout
+ * gradient dqkv [rows][(heads_q + 2 heads_kv) * 128] -- dq and dk turned back
+ * by the transposed rotation
+ *   g_i = bf16(fl32(fl32(a_i c) + fl32(a_{i+64} s))),
+ *   g_{i+64} = bf16(fl32(fl32(a_{i+64} c) - fl32(a_i s))),
+ * dv copied -- and quantizes it in the same pass under `route` into the
+ * views requested (row view with FP4_FLAG_SR_ROW semantics under sr_seed /
+ * sr_offset when `sr` is non-zero: the QKV Dgrad operand; column view: the
+ * QKV Wgrad operand).  dqkv_tap (optional, device bf16 [rows][...]) receives
+ * the gradient that was quantized.  workspace: fp4_quantize_workspace_bytes()
+ * bytes for (route, rows, (heads_q + 2 heads_kv) * 128).  Errors as
+ * fp4_quantize. */
+FP4_API int fp4_qkv_rope_bwd(int route, unsigned views, int sr, const void* dq, const void* dk, const void* dv,
+                             const float* rope_cos, const float* rope_sin, int64_t rows, int64_t seq_len, int heads_q,
+                             int heads_kv, uint64_t sr_seed, uint64_t sr_offset, void* dqkv_tap,
+                             fp4_tensor* dqkv_row, fp4_tensor* dqkv_col, void* workspace, size_t workspace_bytes,
+                             fp4_stream_t stream);
 
 /* Fused gated-FFN forward producer (Sec. 3.2).  One contraction over the
  * paired projections,

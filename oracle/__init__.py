@@ -92,6 +92,11 @@ def _declare(L):
         "orc_hadamard32_f32": (None, [_f32p, _i8p]),
         "orc_hadamard32_rows": (None, [_f32p, _i64, _i64, _i8p]),
         "orc_hadamard16_f32": (None, [_f32p, _i8p]),
+        "orc_rope_tables": (None, [_i64, ctypes.c_int, ctypes.c_double, _f32p, _f32p]),
+        "orc_qkv_rope_fwd": (None, [_u16p, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p, _f32p,
+                                    _u16p, _u16p, _u16p]),
+        "orc_qkv_rope_bwd": (None, [_u16p, _u16p, _u16p, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    _f32p, _f32p, _u16p]),
         "orc_hadamard16_rows": (None, [_f32p, _i64, _i64, _i8p]),
         "orc_sylvester_h32": (None, [_i8p]),
         "orc_mx_quantize_rows": (None, [_f32p, _i64, _i64, ctypes.c_int, _u64, _u64, _u64, _i64, _u8p, _u8p]),
@@ -443,3 +448,47 @@ def rmsnorm_bwd(dy, rp, rstd, g, dres):
     lib().orc_rmsnorm_bwd(_p(dy, _u16p), _p(rp, _u16p), _p(rstd, _f32p), _p(g, _u16p), _p(dres, _u16p), R, C,
                           _p(dr, _u16p))
     return dr
+
+
+# ---------------------------------------------------------------------------
+# QKV producer with RoPE (Sec. 3.2)
+# ---------------------------------------------------------------------------
+
+ROPE_THETA = 500000.0  # Llama-3's base (the pages name RoPE but not its constants)
+
+
+def rope_tables(S: int, D: int = 128, theta: float = ROPE_THETA):
+    """cos, sin of p * theta^(-2i/D), binary64 rounded to binary32, [S][D/2] each."""
+    c = np.empty((S, D // 2), np.float32)
+    s_ = np.empty((S, D // 2), np.float32)
+    lib().orc_rope_tables(S, D, theta, _p(c, _f32p), _p(s_, _f32p))
+    return c, s_
+
+
+def qkv_rope_fwd(qkv: np.ndarray, S: int, hq: int, hkv: int, cos_t, sin_t, D: int = 128):
+    """qkv [T][(hq + 2 hkv) D] bf16 bits -> head-major q [hq][T][D], k, v
+    [hkv][T][D]: Q and K turned by RoPE (rotate-half pairs, binary32 then
+    bf16), V copied."""
+    qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
+    T = qkv.shape[0]
+    assert qkv.shape[1] == (hq + 2 * hkv) * D
+    q = np.empty((hq, T, D), np.uint16)
+    k = np.empty((hkv, T, D), np.uint16)
+    v = np.empty((hkv, T, D), np.uint16)
+    c, s_ = (np.ascontiguousarray(x, dtype=np.float32) for x in (cos_t, sin_t))
+    lib().orc_qkv_rope_fwd(_p(qkv, _u16p), T, S, hq, hkv, D, _p(c, _f32p), _p(s_, _f32p), _p(q, _u16p), _p(k, _u16p),
+                           _p(v, _u16p))
+    return q, k, v
+
+
+def qkv_rope_bwd(dq: np.ndarray, dk: np.ndarray, dv: np.ndarray, S: int, cos_t, sin_t, D: int = 128):
+    """Head-major gradients of the turned Q, K and of V -> dqkv [T][(hq + 2 hkv) D]
+    (the transposed rotation on dQ, dK; dV copied)."""
+    dq, dk, dv = (np.ascontiguousarray(x, dtype=np.uint16) for x in (dq, dk, dv))
+    hq, T, _ = dq.shape
+    hkv = dk.shape[0]
+    out = np.empty((T, (hq + 2 * hkv) * D), np.uint16)
+    c, s_ = (np.ascontiguousarray(x, dtype=np.float32) for x in (cos_t, sin_t))
+    lib().orc_qkv_rope_bwd(_p(dq, _u16p), _p(dk, _u16p), _p(dv, _u16p), T, S, hq, hkv, D, _p(c, _f32p),
+                           _p(s_, _f32p), _p(out, _u16p))
+    return out

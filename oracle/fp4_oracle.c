@@ -594,3 +594,86 @@ void orc_rmsnorm_bwd(const uint16_t* dy, const uint16_t* rp, const float* rstd, 
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* QKV producer with RoPE ("Format-Aware Fusion for Fast FP4 Pretraining",   */
+/* Sec. 3.2: the Q/K projection applies RoPE and the attention layout; the   */
+/* backward combines the inverse layout and RoPE with the QKV gradient        */
+/* production).  Readings: Llama-3 heads of D values, the QKV columns laid    */
+/* out [Q heads | K heads | V heads]; rotate-half pairs (i, i + D/2) turned   */
+/* by p * theta^(-2i/D) at position p = token mod S; the outputs head-major   */
+/* [heads][T][D].                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* cos/sin of p * theta^(-2i/D) for p < S, i < D/2 in binary64, rounded to
+ * binary32 ([S][D/2] each). */
+void orc_rope_tables(int64_t S, int D, double theta, float* cos_t, float* sin_t)
+{
+    const int h = D / 2;
+    for (int64_t p = 0; p < S; ++p)
+        for (int i = 0; i < h; ++i) {
+            double a = (double)p * pow(theta, -2.0 * (double)i / (double)D);
+            cos_t[p * h + i] = (float)cos(a);
+            sin_t[p * h + i] = (float)sin(a);
+        }
+}
+
+/* One head of D bf16 values turned by the angles of one position (c, s of
+ * D/2 each); binary32 products and sums, then bf16.  inverse != 0 applies
+ * the transposed rotation (the gradient's). */
+static void rope_head(const uint16_t* x, const float* c, const float* s, int D, int inverse, uint16_t* y)
+{
+    const int h = D / 2;
+    for (int i = 0; i < h; ++i) {
+        float a = bf16_value(x[i]), b = bf16_value(x[i + h]);
+        float ac = a * c[i], bs = b * s[i], bc = b * c[i], as = a * s[i];
+        float lo = inverse ? ac + bs : ac - bs;
+        float hi = inverse ? bc - as : bc + as;
+        y[i] = orc_bf16_round((double)lo);
+        y[i + h] = orc_bf16_round((double)hi);
+    }
+}
+
+/* Forward: qkv [T][(hq + 2 hkv) D] bf16 -> q [hq][T][D], k [hkv][T][D]
+ * (turned), v [hkv][T][D] (copied). */
+void orc_qkv_rope_fwd(const uint16_t* qkv, int64_t T, int64_t S, int hq, int hkv, int D, const float* cos_t,
+                      const float* sin_t, uint16_t* q, uint16_t* k, uint16_t* v)
+{
+    const int64_t N = (int64_t)(hq + 2 * hkv) * D;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t p = t % S;
+        const float* c = cos_t + p * (D / 2);
+        const float* s = sin_t + p * (D / 2);
+        for (int hd = 0; hd < hq + 2 * hkv; ++hd) {
+            const uint16_t* src = qkv + t * N + (int64_t)hd * D;
+            if (hd < hq)
+                rope_head(src, c, s, D, 0, q + ((int64_t)hd * T + t) * D);
+            else if (hd < hq + hkv)
+                rope_head(src, c, s, D, 0, k + ((int64_t)(hd - hq) * T + t) * D);
+            else
+                for (int i = 0; i < D; ++i) v[((int64_t)(hd - hq - hkv) * T + t) * D + i] = src[i];
+        }
+    }
+}
+
+/* Backward: dq [hq][T][D], dk, dv [hkv][T][D] -> dqkv [T][(hq + 2 hkv) D]
+ * (dq, dk turned back, dv copied). */
+void orc_qkv_rope_bwd(const uint16_t* dq, const uint16_t* dk, const uint16_t* dv, int64_t T, int64_t S, int hq,
+                      int hkv, int D, const float* cos_t, const float* sin_t, uint16_t* dqkv)
+{
+    const int64_t N = (int64_t)(hq + 2 * hkv) * D;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t p = t % S;
+        const float* c = cos_t + p * (D / 2);
+        const float* s = sin_t + p * (D / 2);
+        for (int hd = 0; hd < hq + 2 * hkv; ++hd) {
+            uint16_t* dst = dqkv + t * N + (int64_t)hd * D;
+            if (hd < hq)
+                rope_head(dq + ((int64_t)hd * T + t) * D, c, s, D, 1, dst);
+            else if (hd < hq + hkv)
+                rope_head(dk + ((int64_t)(hd - hq) * T + t) * D, c, s, D, 1, dst);
+            else
+                for (int i = 0; i < D; ++i) dst[i] = dv[((int64_t)(hd - hq - hkv) * T + t) * D + i];
+        }
+    }
+}

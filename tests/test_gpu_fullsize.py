@@ -310,3 +310,53 @@ def test_operand_hybrid_w1_full():
     check_sampled(Y, ov["xr"], ov["wr"], "hybrid Fprop (MX)", rng)
     check_sampled(DX, ov["dr"], ov["wc"], "hybrid Dgrad (CTA-local)", rng)
     check_sampled(DW, ov["dc"], ov["xc"], "hybrid Wgrad (MX, H16 pair)", rng)
+
+
+# ------------------------------------------------- QKV producer with RoPE ----
+def test_qkv_rope_full():
+    """The Llama-3-8B QKV boundary (T 8192, d 4096, 32 query and 8 key/value
+    heads of 128, sequences of 4096): the fused forward on sampled 128-row
+    blocks against the oracle's binary64 contraction turned in binary64, and
+    the backward producer's gradient and CTA-local views bit for bit."""
+    T, d, hq, hkv, S, route = 8192, 4096, 32, 8, 4096, "nv_local"
+    N = (hq + 2 * hkv) * 128
+    x = normal_bf16((T, d), 1.0, 95, 1)
+    w = normal_bf16((N, d), 0.02, 95, 2)
+    xr, _ = F.fp4_quantize(to_dev(x), route, F.FP4_VIEW_ROW)
+    wr, _ = F.fp4_quantize(to_dev(w), route, F.FP4_VIEW_ROW, F.FP4_FLAG_WEIGHT_2D)
+    c, s = oracle.rope_tables(S, 128)
+    cd, sd = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+    q, k, v = F.fp4_qkv_rope_fwd(xr, wr, cd, sd, S, hq, hkv)
+    torch.cuda.synchronize()
+    assert F.fp4_status() == F.FP4_OK
+    ox, ow = oracle.quantize(x, route, "row"), oracle.quantize(w, route, "row", weight2d=True)
+    same_view(xr, ox, "X row")
+    rng = np.random.default_rng(14)
+    for _ in range(2):
+        t0 = int(rng.integers(0, T // 128)) * 128
+        mm, nn = np.meshgrid(np.arange(t0, t0 + 128), np.arange(N), indexing="ij")
+        ref, absref = oracle.gemm_sampled(ox, ow, mm.ravel(), nn.ravel())
+        ref, absref = ref.reshape(128, N), absref.reshape(128, N)
+        pos = np.arange(t0, t0 + 128) % S
+        cp, sp = c[pos].astype(np.float64), s[pos].astype(np.float64)
+        for h in (0, hq - 1, hq, hq + hkv - 1):  # first and last query and key heads
+            a, b = ref[:, h * 128:h * 128 + 64], ref[:, h * 128 + 64:(h + 1) * 128]
+            aa, ab = absref[:, h * 128:h * 128 + 64], absref[:, h * 128 + 64:(h + 1) * 128]
+            want = np.concatenate([a * cp - b * sp, b * cp + a * sp], axis=1)
+            mag = np.concatenate([np.abs(a) * np.abs(cp) + np.abs(b) * np.abs(sp),
+                                  np.abs(b) * np.abs(cp) + np.abs(a) * np.abs(sp)], axis=1)
+            tol = np.concatenate([aa * np.abs(cp) + ab * np.abs(sp), ab * np.abs(cp) + aa * np.abs(sp)], axis=1)
+            src = q[h] if h < hq else k[h - hq]
+            got = oracle.bf16_to_f32(bits(src[t0:t0 + 128])).astype(np.float64)
+            assert (np.abs(got - want) <= 2.0 ** -7 * mag + 2.0 ** -17 * tol + 1e-30).all(), f"head {h}"
+    del q, k, v
+    dq = normal_bf16((hq, T, 128), 1e-4, 96, 1)
+    dk = normal_bf16((hkv, T, 128), 1e-4, 96, 2)
+    dv = normal_bf16((hkv, T, 128), 1e-4, 96, 3)
+    rr, cc = F.fp4_qkv_rope_bwd(to_dev(dq), to_dev(dk), to_dev(dv), cd, sd, S, route, 3, sr=True, sr_seed=6,
+                                sr_offset=0)
+    torch.cuda.synchronize()
+    assert F.fp4_status() == F.FP4_OK
+    want = oracle.qkv_rope_bwd(dq, dk, dv, S, c, s)
+    same_view(rr, oracle.quantize(want, route, "row", sr=True, seed=6, offset=0), "dQKV row")
+    same_view(cc, oracle.quantize(want, route, "col"), "dQKV col")
