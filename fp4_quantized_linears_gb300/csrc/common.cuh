@@ -58,15 +58,18 @@ FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
 FP4_DEV uint32_t e2m1_sr(float v, uint32_t u16) {
     const uint32_t bits = __float_as_uint(v);
     const uint32_t a = bits & 0x7FFFFFFFu;
-    const uint32_t sign = (bits >> 28) & 8u;
-    const uint32_t hi_code = (a >> 22) - 252u + ((u16 << 6) < (a & 0x3FFFFFu) ? 1u : 0u);
+    // |v| in [1, 6): adding 2^22 - 1 - u * 2^6 (the 22-bit complement of the
+    // aligned uniform) to the bits carries into the grid bit exactly when
+    // u * 2^6 < low22, i.e. when the value rounds up; saturate at code 7
+    const uint32_t hi_code = min(((a + ((u16 << 6) ^ 0x3FFFFFu)) >> 22) - 252u, 7u);
+    // |v| < 1: t = |v| * 2^17 (exact), q- index = (t >= 2^16); round up iff
+    // u + index * 2^16 < t, the left side formed as a float through 2^23
     const float t = __fmul_rn(__uint_as_float(a), 131072.0f);
     const uint32_t lo_idx = t >= 65536.0f ? 1u : 0u;
-    const float tt = __fsub_rn(t, lo_idx ? 65536.0f : 0.0f);
-    const uint32_t lo_code = lo_idx + ((float)u16 < tt ? 1u : 0u);
-    uint32_t code = a >= 0x3F800000u ? hi_code : lo_code;
-    code = a >= 0x40C00000u ? 7u : code;  // |v| >= 6 saturates
-    return sign | code;
+    const float uf = __fsub_rn(__uint_as_float(0x4B000000u | u16 | (lo_idx << 16)), 8388608.0f);
+    const uint32_t lo_code = lo_idx + (uf < t ? 1u : 0u);
+    const uint32_t code = a >= 0x3F800000u ? hi_code : lo_code;
+    return ((bits >> 28) & 8u) | code;
 }
 
 // --------------------------------------------------------------- E4M3 ------
@@ -115,6 +118,33 @@ FP4_DEV uint32_t nv_block_scale(float block_amax, float senc, float& mult) {
     float s_raw = __fmul_rn(__fdiv_rn(block_amax, 6.0f), senc);
     uint32_t d = e4m3_rn_satfinite(s_raw);
     mult = d == 0 ? 0.0f : __fdiv_rn(senc, e4m3_value(d));
+    return d;
+}
+
+// ----------------------------------------------------- packed binary32 ----
+// Two binary32 lanes per instruction (f32x2 arithmetic of sm_100 and later):
+// each lane is the round-to-nearest-even result of the scalar operation on
+// that lane, so a pair op and two scalar ops give the same bits.
+FP4_DEV void f32x2_add(float& x, float& y, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+FP4_DEV void f32x2_sub(float& x, float& y, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+FP4_DEV void f32x2_mul(float& x, float& y, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max(m, |a|, |b|), NaN if any operand is NaN (so a NaN input still reaches
+// the non-finite check through the block maximum).
+FP4_DEV float max3_abs_nan(float m, float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
     return d;
 }
 

@@ -58,25 +58,24 @@ FP4_DEV int col_stage_off(int c, int j) { return j * 2048 + ((c ^ j) << 4); }
 // Byte offset of local block j (0..nb-1) of local row r in staged atoms.
 FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
 
-FP4_DEV uint32_t amax_bits32(const float* v) {
-    uint32_t m = 0;
+// fp32 bits of max |v[i]| over n values (non-negative, so the float and the
+// bit order agree; a NaN anywhere gives a NaN, caught by check_finite).
+template <int N>
+FP4_DEV uint32_t amax_bits(const float* v) {
+    float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-    return m;
+    for (int i = 0; i < N; i += 2) m = max3_abs_nan(m, v[i], v[i + 1]);
+    return __float_as_uint(m);
 }
-FP4_DEV uint32_t amax_bits16(const float* v) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-    return m;
-}
+FP4_DEV uint32_t amax_bits32(const float* v) { return amax_bits<32>(v); }
+FP4_DEV uint32_t amax_bits16(const float* v) { return amax_bits<16>(v); }
 // Packed per-half maximum of |bf16| over n bf16x2 words (bits of the low and
 // high halves' maxima in the two 16-bit lanes).
 template <int N>
 FP4_DEV uint32_t amax_words(const uint32_t* w) {
     uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < N; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+    for (int i = 0; i < N; i += 2) m = __vimax3_u16x2(m, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
     return m;
 }
 // fp32 bit pattern of a bf16 magnitude held in a 16-bit lane.
@@ -93,7 +92,9 @@ FP4_DEV uint4 pack_rn32(const float* v, float m0, float m1) {
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             int i = q * 8 + b * 2;
-            word |= e2m1x2_rn(__fmul_rn(v[i], mult), __fmul_rn(v[i + 1], mult)) << (8 * b);
+            float x, y;
+            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
+            word |= e2m1x2_rn(x, y) << (8 * b);
         }
         w[q] = word;
     }
@@ -112,8 +113,10 @@ FP4_DEV uint4 pack_sr32(const float* v, float m0, float m1, uint64_t g0, uint64_
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             int i = q * 8 + b * 2;
-            uint32_t c0 = e2m1_sr(__fmul_rn(v[i], mult), rw[b] & 0xFFFFu);
-            uint32_t c1 = e2m1_sr(__fmul_rn(v[i + 1], mult), rw[b] >> 16);
+            float x, y;
+            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
+            uint32_t c0 = e2m1_sr(x, rw[b] & 0xFFFFu);
+            uint32_t c1 = e2m1_sr(y, rw[b] >> 16);
             word |= (c0 | (c1 << 4)) << (8 * b);
         }
         w[q] = word;
@@ -121,43 +124,49 @@ FP4_DEV uint4 pack_sr32(const float* v, float m0, float m1, uint64_t g0, uint64_
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Butterfly stages of strides 1 .. H/2 on each H-value group of 32
+// registers.  Stride 1 pairs the two lanes of a register pair (v[2i],
+// v[2i + 1]) and runs scalar; every wider stride pairs whole register pairs
+// and runs on f32x2 lanes.
+template <int H>
+FP4_DEV void butterflies(float* v) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float a = v[j], b = v[j + 1];
+        v[j] = __fadd_rn(a, b);
+        v[j + 1] = __fsub_rn(a, b);
+    }
+#pragma unroll
+    for (int h = 2; h < H; h <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            if ((j & h) == 0) {
+                const float a0 = v[j], a1 = v[j + 1], b0 = v[j + h], b1 = v[j + h + 1];
+                f32x2_add(v[j], v[j + 1], a0, a1, b0, b1);
+                f32x2_sub(v[j + h], v[j + h + 1], a0, a1, b0, b1);
+            }
+        }
+    }
+}
+FP4_DEV void scale_all(float* v, float s) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) f32x2_mul(v[i], v[i + 1], v[i], v[i + 1], s, s);
+}
+
 // H32 butterflies on 32 registers whose fixed signs were already applied:
 // stages of stride 1, 2, 4, 8 within each 16-value half, then the cross-half
 // stage of stride 16, then the binary32 multiply by fl32(1/sqrt(32)).
 FP4_DEV void hadamard32_nosign(float* v) {
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if ((j & h) == 0) {
-                float a = v[j], b = v[j + h];
-                v[j] = __fadd_rn(a, b);
-                v[j + h] = __fsub_rn(a, b);
-            }
-        }
-    }
-    const float s = __uint_as_float(0x3E3504F3u);  // fl32(1 / sqrt(32))
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], s);
+    butterflies<32>(v);
+    scale_all(v, __uint_as_float(0x3E3504F3u));  // fl32(1 / sqrt(32))
 }
 
 // H16 butterflies on each 16-value half of 32 registers whose fixed signs
 // were already applied: stages of stride 1, 2, 4, 8, then the multiply by
 // 1/sqrt(16) = 0.25 (exact).
 FP4_DEV void hadamard16x2_nosign(float* v) {
-#pragma unroll
-    for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if ((j & h) == 0) {
-                float a = v[j], b = v[j + h];
-                v[j] = __fadd_rn(a, b);
-                v[j + h] = __fsub_rn(a, b);
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+    butterflies<16>(v);
+    scale_all(v, 0.25f);
 }
 
 // Load the 128x128 tile at (r0, c0) into shared memory (row stride LDS),
