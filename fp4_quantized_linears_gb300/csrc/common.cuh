@@ -46,30 +46,70 @@ FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
     return r;
 }
 
+// ----------------------------------------------------- packed binary32 ----
+// Two binary32 lanes per instruction (f32x2 arithmetic of sm_100 and later):
+// each lane is the correctly rounded result of the scalar operation on
+// that lane (to nearest even, or upward for add_rp), so a pair op and two scalar ops give the same bits.
+FP4_DEV void f32x2_add(float& x, float& y, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+FP4_DEV void f32x2_sub(float& x, float& y, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+FP4_DEV void f32x2_add_rp(float& x, float& y, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rp.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+FP4_DEV void f32x2_fma(float& x, float& y, float a0, float a1, float b0, float b1, float c0, float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+FP4_DEV void f32x2_mul(float& x, float& y, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max(m, |a|, |b|), NaN if any operand is NaN (so a NaN input still reaches
+// the non-finite check through the block maximum).
+FP4_DEV float max3_abs_nan(float m, float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+    return d;
+}
+
 // --------------------------------------------------------------- E2M1 SR ---
 // Adjacent-bin stochastic rounding (Sec. 2.5, Eq. 9): with q- <= |v| < q+
-// neighbouring grid values, round up iff u * 2^-16 < p = (|v| - q-) / (q+ - q-);
-// |v| >= 6 saturates.  Evaluated exactly on the binary32 bits of |v|:
-//   |v| in [1, 6): the grid has one fraction bit, so q- is the value
-//     truncated to one fraction bit (index (bits >> 22) - 252) and
-//     p = (22 low fraction bits) / 2^22, i.e. up iff u << 6 < low22;
-//   |v| < 1: spacing 0.5, t = |v| * 2^17 (exact), q- index = (t >= 2^16),
-//     p * 2^16 = t - index * 2^16 (exact), up iff u < p * 2^16.
-FP4_DEV uint32_t e2m1_sr(float v, uint32_t u16) {
-    const uint32_t bits = __float_as_uint(v);
-    const uint32_t a = bits & 0x7FFFFFFFu;
-    // |v| in [1, 6): adding 2^22 - 1 - u * 2^6 (the 22-bit complement of the
-    // aligned uniform) to the bits carries into the grid bit exactly when
-    // u * 2^6 < low22, i.e. when the value rounds up; saturate at code 7
-    const uint32_t hi_code = min(((a + ((u16 << 6) ^ 0x3FFFFFu)) >> 22) - 252u, 7u);
-    // |v| < 1: t = |v| * 2^17 (exact), q- index = (t >= 2^16); round up iff
-    // u + index * 2^16 < t, the left side formed as a float through 2^23
-    const float t = __fmul_rn(__uint_as_float(a), 131072.0f);
-    const uint32_t lo_idx = t >= 65536.0f ? 1u : 0u;
-    const float uf = __fsub_rn(__uint_as_float(0x4B000000u | u16 | (lo_idx << 16)), 8388608.0f);
-    const uint32_t lo_code = lo_idx + (uf < t ? 1u : 0u);
-    const uint32_t code = a >= 0x3F800000u ? hi_code : lo_code;
-    return ((bits >> 28) & 8u) | code;
+// neighbouring grid values, round up iff u * 2^-16 < p = (|v| - q-) / (q+ - q-)
+// for a 16-bit uniform u; |v| >= 6 saturates.  Evaluated exactly, two values
+// at a time (u_x = rw & 0xFFFF for x, u_y = rw >> 16 for y):
+//   |v| in [1, 6): the grid has one fraction bit, q- is |v| truncated to it
+//     (code (bits >> 22) - 252) and p = low22 / 2^22 (the 22 fraction bits
+//     below it).  Adding 2^22 - 1 - u * 2^6 to the bits carries into the grid
+//     bit exactly when u * 2^6 < low22, i.e. when the value rounds up;
+//   |v| < 1: the grid 0, 0.5, 1 has step 0.5, so the code is
+//     ceil(2|v| - u * 2^-16) = ceil((|v| * 2^17 - u) / 2^16).  The FMA
+//     |v| * 2^17 - u is exact where it can reach 2^16 (|v| >= 0.5) and keeps
+//     its sign elsewhere; a round-upward add of 1.5 * 2^39 (float spacing 2^16
+//     there) takes the ceiling and leaves the code in the low bits.
+FP4_DEV uint32_t e2m1x2_sr(float x, float y, uint32_t rw) {
+    const uint32_t bx = __float_as_uint(x), by = __float_as_uint(y);
+    const uint32_t ax = bx & 0x7FFFFFFFu, ay = by & 0x7FFFFFFFu;
+    const uint32_t hx = min((ax + (((rw << 6) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
+    const uint32_t hy = min((ay + (((rw >> 10) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
+    float nx, ny, zx, zy;
+    f32x2_sub(nx, ny, 8388608.0f, 8388608.0f, __uint_as_float(__byte_perm(rw, 0x4B000000u, 0x7610)),
+              __uint_as_float(__byte_perm(rw, 0x4B000000u, 0x7632)));  // -u_x, -u_y (exact)
+    f32x2_fma(zx, zy, __uint_as_float(ax), __uint_as_float(ay), 131072.0f, 131072.0f, nx, ny);
+    f32x2_add_rp(zx, zy, zx, zy, 824633720832.0f, 824633720832.0f);  // 1.5 * 2^39 = 0x53400000
+    const uint32_t cx = ax >= 0x3F800000u ? hx : __float_as_uint(zx) - 0x53400000u;
+    const uint32_t cy = ay >= 0x3F800000u ? hy : __float_as_uint(zy) - 0x53400000u;
+    return (cx | ((bx >> 28) & 8u)) | ((cy | ((by >> 28) & 8u)) << 4);
 }
 
 // --------------------------------------------------------------- E4M3 ------
@@ -118,33 +158,6 @@ FP4_DEV uint32_t nv_block_scale(float block_amax, float senc, float& mult) {
     float s_raw = __fmul_rn(__fdiv_rn(block_amax, 6.0f), senc);
     uint32_t d = e4m3_rn_satfinite(s_raw);
     mult = d == 0 ? 0.0f : __fdiv_rn(senc, e4m3_value(d));
-    return d;
-}
-
-// ----------------------------------------------------- packed binary32 ----
-// Two binary32 lanes per instruction (f32x2 arithmetic of sm_100 and later):
-// each lane is the round-to-nearest-even result of the scalar operation on
-// that lane, so a pair op and two scalar ops give the same bits.
-FP4_DEV void f32x2_add(float& x, float& y, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-FP4_DEV void f32x2_sub(float& x, float& y, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-FP4_DEV void f32x2_mul(float& x, float& y, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-// max(m, |a|, |b|), NaN if any operand is NaN (so a NaN input still reaches
-// the non-finite check through the block maximum).
-FP4_DEV float max3_abs_nan(float m, float a, float b) {
-    float d;
-    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
     return d;
 }
 

@@ -341,9 +341,9 @@ FP4_DEV uint32_t mx_block_sr(const float* v, uint64_t g0, uint64_t seed, uint64_
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             int i = q * 8 + b * 2;
-            uint32_t c0 = e2m1_sr(__fmul_rn(v[i], mult), rw[b] & 0xFFFFu);
-            uint32_t c1 = e2m1_sr(__fmul_rn(v[i + 1], mult), rw[b] >> 16);
-            word |= (c0 | (c1 << 4)) << (8 * b);
+            float x, y;
+            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
+            word |= e2m1x2_sr(x, y, rw[b]) << (8 * b);
         }
         w[q] = word;
     }

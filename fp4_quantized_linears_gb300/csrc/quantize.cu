@@ -115,9 +115,7 @@ FP4_DEV uint4 pack_sr32(const float* v, float m0, float m1, uint64_t g0, uint64_
             int i = q * 8 + b * 2;
             float x, y;
             f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
-            uint32_t c0 = e2m1_sr(x, rw[b] & 0xFFFFu);
-            uint32_t c1 = e2m1_sr(y, rw[b] >> 16);
-            word |= (c0 | (c1 << 4)) << (8 * b);
+            word |= e2m1x2_sr(x, y, rw[b]) << (8 * b);
         }
         w[q] = word;
     }
