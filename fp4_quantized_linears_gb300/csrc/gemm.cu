@@ -20,16 +20,18 @@
 //                   FP4 views of [da1 | da3] for the W1/W3 Dgrad (row view,
 //                   stochastic rounding) and Wgrad (column view).
 //
-// Structure: a persistent kernel, one CTA per SM (320 threads), clusters of
+// Structure: a persistent kernel, one CTA per SM (352 threads), clusters of
 // CM CTAs along M that share the B tile through TMA multicast:
 //   warp 0      TMA producer: A tile (128 rows), this CTA's share of the B
 //               tile multicast to the cluster, scale atoms (1D bulk copies),
 //               into a STAGES-deep ring of mbarrier-guarded stages;
-//   warp 1      owns the TMEM allocation; one thread copies each stage's
-//               scale atoms into TMEM (tcgen05.cp 32x128b.warpx4) and issues
-//               the block-scaled MMAs (kind::mxf4 E8M0 / kind::mxf4nvf4 E4M3)
-//               into a 128 x BN FP32 accumulator; the stage is released to
-//               every CTA of the cluster by a multicast tcgen05.commit;
+//   warp 1      owns the TMEM allocation; one thread issues the block-scaled
+//               MMAs (kind::mxf4 E8M0 / kind::mxf4nvf4 E4M3) into a
+//               128 x BN FP32 accumulator; the stage is released to every
+//               CTA of the cluster by a multicast tcgen05.commit;
+//   warp 10     one thread copies each landed stage's scale atoms into TMEM
+//               (tcgen05.cp 32x128b.warpx4) ahead of the MMA thread, which
+//               waits for the copies' commit instead of the landing;
 //   warps 2-9   epilogue: drain the accumulator from TMEM into registers
 //               (each warp one lane quarter x one column half), release it so
 //               the next tile's MMAs start, then finish the tile while the
@@ -62,8 +64,9 @@ constexpr int BK = 256;  // FP4 elements per stage: 128-byte rows, 128-byte swiz
 constexpr int BK_BYTES = BK / 2;
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
 constexpr int MAX_STAGES = 8;
-constexpr int THREADS = 320;
 constexpr int EPI_WARPS = 8;
+constexpr int SF_WARP = 2 + EPI_WARPS;  // the warp that moves scale factors into TMEM
+constexpr int THREADS = 32 * (SF_WARP + 1);
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;  // first TMEM column of the scale-factor region
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
@@ -446,7 +449,7 @@ struct Cfg {
     static_assert(STAGES >= 3, "pipeline depth");
     static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
-    static_assert(2 * MAX_STAGES * 8 + 64 <= 256, "barrier area");
+    static_assert(3 * MAX_STAGES * 8 + 64 <= 256, "barrier area");
 };
 
 template <bool NV, int BN, int EPI, int CM, bool P2 = false>
@@ -464,11 +467,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::STAGING);
     uint64_t* empty = full + STAGES;
-    uint64_t* acc_full = empty + STAGES;
+    uint64_t* sf_full = empty + STAGES;   // the stage's scale factors are in TMEM
+    uint64_t* acc_full = sf_full + STAGES;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* drain_bar = acc_empty + 1;  // MMA completion point at the end
     uint64_t* epi_bar = drain_bar + 1;    // bounded barrier among the epilogue warps
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
+    uint64_t* sf_drain = epi_bar + 1;     // completion point of the last scale-factor copies
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -503,7 +508,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], P2 ? 1 : CM);  // pair: the leader's commit reaches each CTA once
+            mbar_init(&sf_full[s], 1);
         }
+        mbar_init(sf_drain, 1);
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, P2 ? 2 * EPI_WARPS : EPI_WARPS);  // pair: both CTAs' epilogues, on the leader
         mbar_init(drain_bar, 1);
@@ -631,7 +638,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (*abort_flag || !mbar_wait(&full[stage], phase)) {
+                // the stage has landed and its scale factors are in TMEM
+                if (*abort_flag || !mbar_wait(&sf_full[stage], phase)) {
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -639,19 +647,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t sfa_col = sf_base + stage * C::SF_COLS;
                 const uint32_t sfb_col = sfa_col + C::SF_COLS_A;
-                // each chunk's scale atoms go to TMEM (replicated into the four
-                // lane quarters) right before the MMAs that read them
                 const uint32_t a_base = smem_u32(stage_a(stage)), b_base = smem_u32(stage_b(stage));
                 constexpr int MMAS_PER_CHUNK = (BK / 64) / C::SF_CHUNKS;
 #pragma unroll
                 for (int c = 0; c < C::SF_CHUNKS; ++c) {
-                    tc_cp_sf<G>(sfa_col + 4 * c,
-                                smem_desc(smem_u32(stage_sfa(stage) + c * 512), 0, 128, LAYOUT_NONE));
-#pragma unroll
-                    for (int h = 0; h < BN / 128; ++h)
-                        tc_cp_sf<G>(sfb_col + c * (BN / 32) + 4 * h,
-                                    smem_desc(smem_u32(stage_sfb(stage) + (h * C::SF_CHUNKS + c) * 512), 0, 128,
-                                              LAYOUT_NONE));
 #pragma unroll
                     for (int q = 0; q < MMAS_PER_CHUNK; ++q) {
                         const int kk = c * MMAS_PER_CHUNK + q;
@@ -691,7 +690,51 @@ __global__ void __launch_bounds__(THREADS, 1)
         // epilogue wait on acc_full can see an extra phase)
         tc_commit<G>(drain_bar);
         mbar_wait(drain_bar, 0);
-    } else if (warp >= 2) {
+    } else if (warp == SF_WARP && lane == 0 && (!P2 || rank == 0)) {
+        // ------------------------------------------------ scale factors ---
+        // Each landed stage's scale atoms go to that stage's TMEM columns
+        // (replicated into the four lane quarters), issued from this thread
+        // so that the copies run beside the MMAs of earlier stages rather
+        // than in the MMA thread's in-order stream; the commit on sf_full
+        // tells the MMA thread they are complete.  Region `stage` is free
+        // again once the stage lands anew: the producer refills it only after
+        // the MMAs that read the previous copies have completed.
+        // (pair: the leader copies for both CTAs, each from its own stage)
+        const uint32_t sf_base = tmem + SF_COL0;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t u = cluster_id; u < n_units && ok; u += n_clusters) {
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (*abort_flag || !mbar_wait(&full[stage], phase)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sfa_col = sf_base + stage * C::SF_COLS;
+                const uint32_t sfb_col = sfa_col + C::SF_COLS_A;
+#pragma unroll
+                for (int c = 0; c < C::SF_CHUNKS; ++c) {
+                    tc_cp_sf<G>(sfa_col + 4 * c,
+                                smem_desc(smem_u32(stage_sfa(stage) + c * 512), 0, 128, LAYOUT_NONE));
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        tc_cp_sf<G>(sfb_col + c * (BN / 32) + 4 * h,
+                                    smem_desc(smem_u32(stage_sfb(stage) + (h * C::SF_CHUNKS + c) * 512), 0, 128,
+                                              LAYOUT_NONE));
+                }
+                tc_commit<G>(&sf_full[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // every copy issued has completed before TMEM can be released
+        tc_commit<G>(sf_drain);
+        mbar_wait(sf_drain, 0);
+    } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
         // ------------------------------------------------ epilogue --------
         const int q = warp & 3;               // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;     // column half
