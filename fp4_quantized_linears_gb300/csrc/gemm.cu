@@ -1394,9 +1394,10 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     const bool wide = (g.N % 256) == 0;
     const int64_t units_1 = (g.M / BM) * (g.N / (wide ? 256 : 128));
     if (g.nv) {
-        // NVFP4 stays on the CTA-multicast kernel: its twice-as-many scale copies made
-        // the pair kernel slower there (measured), while MXFP4 gains 5-10% from it
-        if (wide) return pair ? launch_t<true, 256, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+        // 256-wide tiles go to the CTA-pair kernel for both formats; with the
+        // scale copies off the MMA thread, NVFP4's twice-as-many copies no
+        // longer make it slower than the multicast kernel (10-12% faster)
+        if (wide) return pair ? launch_t<true, 256, EPI_STORE, 2, true>(g, kp, units_1 / 2, stream)
                               : launch_t<true, 256, EPI_STORE, 1>(g, kp, units_1, stream);
         return pair ? launch_t<true, 128, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
                     : launch_t<true, 128, EPI_STORE, 1>(g, kp, units_1, stream);
