@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
                     const __grid_constant__ CUtensorMap tmSB, KParams p) {
     using C = Cfg<NV, BN, EPI, P2>;
-    static_assert(!P2 || (CM == 2 && EPI == EPI_STORE && BN == 256), "pair mode: plain-store 256-wide tiles");
+    static_assert(!P2 || (CM == 2 && BN == 256 && EPI != EPI_SWIGLU_BWD), "pair mode: 256-wide tiles");
     constexpr int G = P2 ? 2 : 1;       // tcgen05 CTA group
     constexpr int MMA_M = P2 ? 2 * BM : BM;
     constexpr int STAGES = C::STAGES;
@@ -646,12 +646,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t fb = mapa_rank(smem_u32(&full[stage]), 0);
                     if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::TX_BYTES);
                     tma_load_2d_pair(stage_a(stage), &tmA, kb * BK_BYTES, (int)m0, fb);
-                    tma_load_2d_pair(stage_b(stage), &tmB, kb * BK_BYTES, (int)(n0 + 128 * rank), fb);
+                    tma_load_2d_pair(stage_b(stage), &tmB, kb * BK_BYTES, (int)b_row(n0, (int)rank), fb);
                     tma_load_2d_pair(stage_sfa(stage), &tmSA, 0, (int)((m0 >> 7) * k_atoms + kb * C::SF_CHUNKS), fb);
 #pragma unroll
                     for (int h = 0; h < BN / 128; ++h)
                         tma_load_2d_pair(stage_sfb(stage) + h * C::SF_CHUNKS * 512, &tmSB, 0,
-                                         (int)(((n0 >> 7) + h) * k_atoms + kb * C::SF_CHUNKS), fb);
+                                         (int)((b_row(n0, h) >> 7) * k_atoms + kb * C::SF_CHUNKS), fb);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -818,6 +818,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int et = (warp - 2) * 32 + lane;  // epilogue thread index 0..255
         uint32_t acc_phase = 0, epi_phase = 0;
         bool epi_ok = true;
+        // the accumulator is free once every epilogue warp has read it; in
+        // pair mode the MMA thread waits on the leader's barrier for the
+        // warps of both CTAs
+        auto release_acc = [&]() {
+            if (lane == 0) {
+                if (P2 && rank != 0)
+                    mbar_arrive_cluster(mapa_rank(smem_u32(acc_empty), 0));
+                else
+                    mbar_arrive(acc_empty);
+            }
+        };
         // bounded barrier among the 256 epilogue threads
         auto epi_sync = [&]() {
             mbar_arrive(epi_bar);
@@ -846,12 +857,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 else
                     tmem_ld64(lane_base + half * (BN / 2), r);
                 tc_fence_before();
-                if (lane == 0) {
-                    if (P2 && rank != 0)
-                        mbar_arrive_cluster(mapa_rank(smem_u32(acc_empty), 0));
-                    else
-                        mbar_arrive(acc_empty);
-                }
+                release_acc();
                 float sa = 1.0f;
                 if (NV) sa = __fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]);
                 const bool tma_out = p.beta == 0.0f || p.beta == 1.0f;
@@ -944,7 +950,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     tmem_ld128(lane_base + 128 * half, r);
                     tc_fence_before();
-                    if (lane == 0) mbar_arrive(acc_empty);
+                    release_acc();
                     float alpha = 1.0f;
                     if (NV)
                         alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
@@ -1003,7 +1009,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t r1[64], r3[64];
                     tmem_ld64x2(lane_base + 64 * half, lane_base + 128 + 64 * half, r1, r3);
                     tc_fence_before();
-                    if (lane == 0) mbar_arrive(acc_empty);
+                    release_acc();
                     float alpha = 1.0f;
                     if (NV)
                         alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
@@ -1086,7 +1092,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     tmem_ld64(lane_base + 64 * half, r);
                     tc_fence_before();
-                    if (lane == 0) mbar_arrive(acc_empty);
+                    release_acc();
                     float alpha = 1.0f;
                     if (NV)
                         alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
@@ -1371,17 +1377,17 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     if (g.epi == 1) {  // SwiGLU forward: B = [W1; W3] with 2f rows, output width f
         g.b_rows = 2 * g.f;
         const int64_t units_1 = (g.M / BM) * (g.f / 128);
-        if (g.nv) return pair ? launch_t<true, 256, EPI_SWIGLU_FWD, 2>(g, kp, units_1 / 2, stream)
+        if (g.nv) return pair ? launch_t<true, 256, EPI_SWIGLU_FWD, 2, true>(g, kp, units_1 / 2, stream)
                               : launch_t<true, 256, EPI_SWIGLU_FWD, 1>(g, kp, units_1, stream);
-        return pair ? launch_t<false, 256, EPI_SWIGLU_FWD, 2>(g, kp, units_1 / 2, stream)
+        return pair ? launch_t<false, 256, EPI_SWIGLU_FWD, 2, true>(g, kp, units_1 / 2, stream)
                     : launch_t<false, 256, EPI_SWIGLU_FWD, 1>(g, kp, units_1, stream);
     }
     g.b_rows = g.N;
     if (g.epi == 3) {  // QKV projection with RoPE into head-major outputs
         const int64_t units_1 = (g.M / BM) * (g.N / 256);
-        if (g.nv) return pair ? launch_t<true, 256, EPI_QKV_ROPE, 2>(g, kp, units_1 / 2, stream)
+        if (g.nv) return pair ? launch_t<true, 256, EPI_QKV_ROPE, 2, true>(g, kp, units_1 / 2, stream)
                               : launch_t<true, 256, EPI_QKV_ROPE, 1>(g, kp, units_1, stream);
-        return pair ? launch_t<false, 256, EPI_QKV_ROPE, 2>(g, kp, units_1 / 2, stream)
+        return pair ? launch_t<false, 256, EPI_QKV_ROPE, 2, true>(g, kp, units_1 / 2, stream)
                     : launch_t<false, 256, EPI_QKV_ROPE, 1>(g, kp, units_1, stream);
     }
     if (g.epi == 2) {  // SwiGLU backward: W2 Dgrad, output [M][f]
