@@ -376,15 +376,20 @@ FP4_DEV void tmem_ld128(uint32_t taddr, uint32_t* r) {
 
 
 // ------------------------------------------------------ epilogue helpers --
+// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+FP4_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 constexpr int ST_LDS = 136;  // staging row stride (bf16 elements)
 
 FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
 
 // MX row/column block of 32 values: scale byte and 16 bytes of RN codes.
 FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
-    uint32_t am = 0;
+    float amf = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    for (int i = 0; i < 32; i += 2) amf = max3_abs_nan(amf, v[i], v[i + 1]);
+    const uint32_t am = __float_as_uint(amf);
     if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
     const int e = e8m0_exponent_up(am);
     const float mult = exp2_neg(e);
@@ -395,7 +400,9 @@ FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             int i = q * 8 + b * 2;
-            word |= e2m1x2_rn(__fmul_rn(v[i], mult), __fmul_rn(v[i + 1], mult)) << (8 * b);
+            float x, y;
+            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
+            word |= e2m1x2_rn(x, y) << (8 * b);
         }
         w[q] = word;
     }
@@ -405,9 +412,10 @@ FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
 
 // MX block of 32 values with stochastic rounding (logical indices 8*g0 ..).
 FP4_DEV uint32_t mx_block_sr(const float* v, uint64_t g0, uint64_t seed, uint64_t offset, uint4& packed) {
-    uint32_t am = 0;
+    float amf = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    for (int i = 0; i < 32; i += 2) amf = max3_abs_nan(amf, v[i], v[i + 1]);
+    const uint32_t am = __float_as_uint(amf);
     if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
     const int e = e8m0_exponent_up(am);
     const float mult = exp2_neg(e);
@@ -841,6 +849,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int64_t u = cluster_id; u < n_units && epi_ok; u += n_clusters) {
             int64_t m0, n0;
             unit_coords(u, m0, n0);
+            if constexpr (EPI == EPI_SWIGLU_BWD) {
+                // this thread's retained a1 / a3 (one 128-byte row segment
+                // each) do not depend on the accumulator: start moving them
+                // into L2 while the tile's MMAs run
+                const int64_t off = (m0 + lr) * p.f + n0 + 64 * half;
+                bulk_prefetch_l2(p.a1 + off, 128);
+                bulk_prefetch_l2(p.a3 + off, 128);
+            }
             if (!mbar_wait(acc_full, acc_phase)) {
                 *abort_flag = 1;
                 break;
@@ -1039,7 +1055,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int e = 0; e < 2; ++e) {
                             const float x1 = e ? bf16_hi(w1) : bf16_lo(w1);
                             const float x3 = e ? bf16_hi(w3) : bf16_lo(w3);
-                            const float sl = x1 * __frcp_rn(1.0f + __expf(-x1));
+                            const float sl = x1 * __fdividef(1.0f, 1.0f + __expf(-x1));
                             hv[e] = __fmul_rn(sl, x3);
                         }
                         hp[i] = bf16x2_rn(hv[0], hv[1]);
@@ -1128,7 +1144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 const float x = e ? bf16_hi(w1[j]) : bf16_lo(w1[j]);
                                 const float y = e ? bf16_hi(w3[j]) : bf16_lo(w3[j]);
                                 const float g = e ? bf16_hi(wg) : bf16_lo(wg);
-                                const float sg = __frcp_rn(1.0f + __expf(-x));
+                                const float sg = __fdividef(1.0f, 1.0f + __expf(-x));
                                 const float dsilu = sg * (1.0f + x * (1.0f - sg));
                                 o1[e] = g * y * dsilu;
                                 o3[e] = g * (x * sg);
