@@ -157,8 +157,12 @@ FP4_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, u
         "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar_cluster)
         : "memory");
 }
+// Arrive on a barrier of another CTA of the cluster.  CTA-scope release: the
+// arrive publishes no data, only that this thread's prior tcgen05 work
+// (ordered by tcgen05.fence::before_thread_sync) is done; a cluster-scope
+// release made the arrive wait for the thread's earlier memory traffic.
 FP4_DEV void mbar_arrive_cluster(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // TMA tensor store / reduce-add of a shared-memory box (bulk-group completion).
