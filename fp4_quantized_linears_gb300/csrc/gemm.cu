@@ -36,9 +36,9 @@
 //               (each warp one lane quarter x one column half), release it so
 //               the next tile's MMAs start, then finish the tile while the
 //               tensor core runs the next one: plain outputs go through a
-//               128B-swizzled 32 x 128-byte shared buffer per warp and a TMA
+//               swizzled 32-row shared buffer per warp and a TMA
 //               tensor store (or TMA reduce-add for beta = 1), so every
-//               global write is a full-line bulk transfer.
+//               global write is a bulk transfer of whole 32-byte sectors.
 // Every mbarrier wait is bounded: a wait that runs out sets the sticky status
 // word to FP4_ERR_TIMEOUT, the roles drain what they issued and the CTA
 // returns, releasing its tensor memory.
@@ -520,16 +520,20 @@ struct Cfg {
     static constexpr int SF_COLS_A = SF_CHUNKS * 4;
     static constexpr int SF_COLS_B = SF_CHUNKS * (BN / 32);
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    static constexpr int RESERVED = 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int RESERVED = 256;  // barriers (the dynamic shared base is 1 KiB aligned; checked)
     static constexpr int fit(int staging) {
         return cmin(MAX_STAGES, cmin((SMEM_LIMIT - RESERVED - staging) / STAGE_BYTES, (TMEM_COLS - SF_COL0) / SF_COLS));
     }
-    // STORE: per epilogue warp two 32-row x 128-byte buffers for TMA stores,
-    // or one where two would cost the ring a stage
+    // STORE: each epilogue warp stages 32-row boxes for TMA stores: 128-byte
+    // rows where that costs the ring no stage, else 64-byte rows (twice the
+    // stores); two buffers per warp where the second costs no stage either
+    static constexpr int MAX_STAGES_OUT = fit(EPI_WARPS * 2048);
+    static constexpr int OUT_ROW = fit(EPI_WARPS * 4096) >= MAX_STAGES_OUT ? 128 : 64;  // bytes per box row
+    static constexpr int OUT_BOX = 32 * OUT_ROW;
     static constexpr int OUT_BUFS =
-        EPI != EPI_STORE ? 0 : (fit(EPI_WARPS * 2 * 4096) >= fit(EPI_WARPS * 4096) ? 2 : 1);
+        EPI != EPI_STORE ? 0 : (fit(EPI_WARPS * 2 * OUT_BOX) >= MAX_STAGES_OUT ? 2 : 1);
     static constexpr int STAGING =
-        EPI == EPI_STORE      ? EPI_WARPS * OUT_BUFS * 4096
+        EPI == EPI_STORE      ? EPI_WARPS * OUT_BUFS * OUT_BOX
         : EPI == EPI_QKV_ROPE ? 0
                               : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
     static constexpr int STAGES = fit(STAGING);
@@ -551,7 +555,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int MMA_M = P2 ? 2 * BM : BM;
     constexpr int STAGES = C::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // The ring's 128-byte-swizzled stages need 1 KiB alignment, and the
+    // budget leaves no slack to realign: a kernel whose dynamic shared base
+    // is not aligned reports an error before touching anything (uniform
+    // across the grid, so no CTA is left waiting at a cluster barrier).
+    if ((reinterpret_cast<uintptr_t>(smem_raw) & 1023) != 0) {
+        if (threadIdx.x == 0) set_status(&g_status_gemm, FP4_ERR_CUDA);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::STAGING);
     uint64_t* empty = full + STAGES;
@@ -882,16 +894,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (NV) sa = __fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]);
                 const bool tma_out = p.beta == 0.0f || p.beta == 1.0f;
                 if (tma_out) {
-                    // rows [32q, 32q+32) of the tile through this warp's two
-                    // 128B-swizzled 32 x 128-byte buffers and TMA stores
-                    uint8_t* wbuf = staging + (warp - 2) * C::OUT_BUFS * 4096;
+                    // rows [32q, 32q+32) of the tile through this warp's
+                    // swizzled 32 x OUT_ROW-byte buffers and TMA stores
+                    constexpr int ROW = C::OUT_ROW, WORDS = ROW / 4;  // 32-bit words per box row
+                    uint8_t* wbuf = staging + (warp - 2) * C::OUT_BUFS * C::OUT_BOX;
                     const bool f32 = p.out_dtype == FP4_OUT_F32;
-                    constexpr int NB = NC;  // boxes per thread: fp32 32 cols, bf16 64 cols
+                    constexpr int NB = (BN / 2) / WORDS;  // boxes per thread (fp32; bf16 needs half)
                     const int nbox = f32 ? NB : NB / 2;
 #pragma unroll
                     for (int bi = 0; bi < NB; ++bi) {
                         if (bi >= nbox) break;
-                        uint8_t* buf = wbuf + (C::OUT_BUFS == 2 ? (bi & 1) * 4096 : 0);
+                        uint8_t* buf = wbuf + (C::OUT_BUFS == 2 ? (bi & 1) * C::OUT_BOX : 0);
                         // the store previously issued from this buffer must have read it
                         if (lane == 0) {
                             if (C::OUT_BUFS == 2)
@@ -900,24 +913,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 bulk_wait_read<0>();
                         }
                         __syncwarp();
-                        const int cols = f32 ? 32 : 64;
+                        const int cols = f32 ? WORDS : 2 * WORDS;
                         const int64_t n = n0 + half * (BN / 2) + cols * bi;
                         float alpha = 1.0f;
                         if (NV) alpha = __fmul_rn(sa, __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n >> 7)]));
-                        uint32_t w[32];
+                        uint32_t w[WORDS];
                         if (f32) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(r[32 * bi + i]) * alpha);
+                            for (int i = 0; i < WORDS; ++i)
+                                w[i] = __float_as_uint(__uint_as_float(r[WORDS * bi + i]) * alpha);
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                w[i] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[64 * bi + 2 * i]) * alpha) |
-                                       ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[64 * bi + 2 * i + 1]) * alpha) << 16);
+                            for (int i = 0; i < WORDS; ++i)
+                                w[i] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * WORDS * bi + 2 * i]) * alpha) |
+                                       ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * WORDS * bi + 2 * i + 1]) * alpha)
+                                        << 16);
                         }
+                        // this lane's row: 16-byte chunk k lands at k ^ (row & 7)
+                        // (128B swizzle) or k ^ ((row >> 1) & 3) (64B swizzle)
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            *reinterpret_cast<uint4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                        for (int k = 0; k < ROW / 16; ++k) {
+                            const int sw = ROW == 128 ? (lane & 7) : ((lane >> 1) & 3);
+                            *reinterpret_cast<uint4*>(buf + lane * ROW + ((k ^ sw) << 4)) =
                                 make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                        }
                         fence_proxy_async();
                         __syncwarp();
                         if (lane == 0) {
@@ -1272,16 +1291,18 @@ bool make_sf_map(CUtensorMap* map, const void* scales, int64_t atoms, int chunk)
     return r == CUDA_SUCCESS;
 }
 
-// Row-major output [M][N] (fp32 or bf16), box 128 bytes x 32 rows, 128B swizzle.
-bool make_out_map(CUtensorMap* map, void* c, int64_t M, int64_t N, int out_dtype) {
+// Row-major output [M][N] (fp32 or bf16), box `row_bytes` (128 or 64) x 32
+// rows with the swizzle of that width.
+bool make_out_map(CUtensorMap* map, void* c, int64_t M, int64_t N, int out_dtype, int row_bytes) {
     const bool f32 = out_dtype == FP4_OUT_F32;
     const int es = f32 ? 4 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)(N * es)};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32u};
+    cuuint32_t box[2] = {(cuuint32_t)(row_bytes / es), 32u};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1313,7 +1334,7 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
             !make_sf_map(&tsb, g.b_scales, (g.b_rows / 128) * k_atoms, C::SF_CHUNKS))
             return FP4_ERR_CUDA;
     }
-    if (EPI == EPI_STORE && (g.beta == 0.0f || g.beta == 1.0f) && !make_out_map(&tc, g.c, g.M, g.N, g.out_dtype))
+    if (EPI == EPI_STORE && (g.beta == 0.0f || g.beta == 1.0f) && !make_out_map(&tc, g.c, g.M, g.N, g.out_dtype, C::OUT_ROW))
         return FP4_ERR_CUDA;
     auto kern = fp4_gemm_kernel<NV, BN, EPI, CM, P2>;
     int dev = 0;
