@@ -107,10 +107,14 @@ def _declare(L):
         "fp4_linear_fprop": (ctypes.c_int, [tp, tp, vp, ctypes.c_int, ctypes.c_float, vp]),
         "fp4_linear_dgrad": (ctypes.c_int, [tp, tp, vp, ctypes.c_int, ctypes.c_float, vp]),
         "fp4_linear_wgrad": (ctypes.c_int, [tp, tp, vp, ctypes.c_float, vp]),
+        "fp4_linear_dgrad_rmsnorm": (ctypes.c_int, [tp, tp, vp, vp, vp, vp, vp, vp]),
         "fp4_residual_rmsnorm_fwd": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint, vp, vp, vp, c_i64, c_i64, c_i64,
                                                     ctypes.c_float, vp, vp, tp, tp, vp, vp, c_sz, vp]),
         "fp4_residual_rmsnorm_bwd": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint, ctypes.c_int, vp, vp, vp, vp, vp,
                                                     c_i64, c_i64, c_u64, c_u64, vp, tp, tp, vp, c_sz, vp]),
+        "fp4_residual_rmsnorm_bwd_parts": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint, ctypes.c_int, vp, vp, vp, vp,
+                                                          vp, vp, c_i64, c_i64, c_u64, c_u64, vp, tp, tp, vp, c_sz,
+                                                          vp]),
         "fp4_rmsnorm_bwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int, c_i64, c_i64, ctypes.POINTER(c_sz)]),
         "fp4_swiglu_fwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, tp, tp, vp, vp]),
         "fp4_swiglu_bwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, c_u64, c_u64, tp, tp, vp, vp, vp]),
@@ -281,6 +285,20 @@ def fp4_linear_dgrad(dy_row: QView, w_col: QView, dx: torch.Tensor | None = None
     return dx
 
 
+def fp4_linear_dgrad_rmsnorm(dy_row: QView, w_col: QView, r_prime: torch.Tensor, rstd: torch.Tensor,
+                             g: torch.Tensor, dx: torch.Tensor | None = None, part: torch.Tensor | None = None,
+                             stream=None):
+    """dx = dY . W (bf16) and the adjacent RMSNorm backward's row terms
+    part [rows][cols / 64] (binary32).  Returns (dx, part)."""
+    dx = _out(dy_row, w_col, dx, FP4_OUT_BF16, dy_row.codes.device)
+    if part is None:
+        part = torch.empty((dy_row.rows, w_col.rows // 64), dtype=torch.float32, device=dy_row.codes.device)
+    a, b = dy_row.struct(), w_col.struct()
+    _check(load().fp4_linear_dgrad_rmsnorm(ctypes.byref(a), ctypes.byref(b), _ptr(dx), _ptr(r_prime), _ptr(rstd),
+                                           _ptr(g), _ptr(part), _stream(stream)), "fp4_linear_dgrad_rmsnorm")
+    return dx, part
+
+
 def fp4_linear_wgrad(dy_col: QView, x_col: QView, dw: torch.Tensor | None = None, beta: float = 0.0,
                      stream=None) -> torch.Tensor:
     dw = _out(dy_col, x_col, dw, FP4_OUT_F32, dy_col.codes.device)
@@ -362,6 +380,32 @@ def fp4_residual_rmsnorm_bwd(dy: torch.Tensor, r_prime: torch.Tensor, rstd: torc
                                            ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None,
                                            _ptr(workspace), workspace.numel(), _stream(stream)),
            "fp4_residual_rmsnorm_bwd")
+    _sync_fields(dr_row, rs)
+    _sync_fields(dr_col, cs)
+    return dr, dr_row, dr_col
+
+
+def fp4_residual_rmsnorm_bwd_parts(dy: torch.Tensor, part: torch.Tensor, r_prime: torch.Tensor, rstd: torch.Tensor,
+                                   g: torch.Tensor, dres: torch.Tensor | None, route, views: int = 3, sr: bool = True,
+                                   sr_seed: int = 0, sr_offset: int = 0, dr=None, dr_row=None, dr_col=None,
+                                   workspace=None, stream=None):
+    """fp4_residual_rmsnorm_bwd with the row means from the row terms `part`
+    that fp4_linear_dgrad_rmsnorm wrote for this dy.  Returns (dr, dr_row, dr_col)."""
+    rt = _route(route)
+    R, C = dy.shape
+    dev = dy.device
+    dr = torch.empty((R, C), dtype=torch.bfloat16, device=dev) if dr is None else dr
+    flags = FP4_FLAG_SR_ROW if sr else 0
+    dr_row, dr_col = _views(rt, R, C, views, flags, dev, dr_row, dr_col)
+    if workspace is None:
+        workspace = torch.empty(fp4_rmsnorm_bwd_workspace_bytes(rt, R, C), dtype=torch.uint8, device=dev)
+    rs = dr_row.struct() if dr_row is not None else None
+    cs = dr_col.struct() if dr_col is not None else None
+    _check(load().fp4_residual_rmsnorm_bwd_parts(rt, views, int(sr), _ptr(dy), _ptr(part), _ptr(r_prime),
+                                                 _ptr(rstd), _ptr(g), _ptr(dres), R, C, sr_seed, sr_offset, _ptr(dr),
+                                                 ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None,
+                                                 _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp4_residual_rmsnorm_bwd_parts")
     _sync_fields(dr_row, rs)
     _sync_fields(dr_col, cs)
     return dr, dr_row, dr_col

@@ -199,10 +199,12 @@ int fp4_rmsnorm_bwd_workspace_bytes(int route, int64_t rows, int64_t cols, size_
     return FP4_OK;
 }
 
-int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, const void* r_prime,
-                             const float* rstd, const void* g, const void* dres, int64_t rows, int64_t cols,
-                             uint64_t sr_seed, uint64_t sr_offset, void* dr, fp4_tensor* dr_row, fp4_tensor* dr_col,
-                             void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
+// The residual-RMSNorm backward: the row means from a pass over dy (part
+// NULL) or from the per-block row terms a data-gradient epilogue wrote.
+static int rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, const float* part, const void* r_prime,
+                       const float* rstd, const void* g, const void* dres, int64_t rows, int64_t cols,
+                       uint64_t sr_seed, uint64_t sr_offset, void* dr, fp4_tensor* dr_row, fp4_tensor* dr_col,
+                       void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
     if (!route_ok(route) || rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;
     if (rows % 128 || cols % 128) return FP4_ERR_UNSUPPORTED_SHAPE;
     size_t need = 0;
@@ -219,8 +221,9 @@ int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, 
         return FP4_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float* mean_g = static_cast<float*>(workspace);
-    rc = launch_rmsnorm_bwd_stats(static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(r_prime), rstd,
-                                  static_cast<const uint16_t*>(g), rows, cols, mean_g, s);
+    rc = part ? launch_rms_parts_reduce(part, rows, cols / 64, cols, mean_g, s)
+              : launch_rmsnorm_bwd_stats(static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(r_prime),
+                                         rstd, static_cast<const uint16_t*>(g), rows, cols, mean_g, s);
     if (rc != FP4_OK) return rc;
     p.pre = PRE_RMSNORM_BWD;
     p.rstd = rstd;
@@ -232,7 +235,35 @@ int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, 
     return launch_quantize(p, s);
 }
 
-static int linear(const fp4_tensor* a, const fp4_tensor* b, void* c, int out_dtype, float beta, fp4_stream_t stream) {
+int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const void* dy, const void* r_prime,
+                             const float* rstd, const void* g, const void* dres, int64_t rows, int64_t cols,
+                             uint64_t sr_seed, uint64_t sr_offset, void* dr, fp4_tensor* dr_row, fp4_tensor* dr_col,
+                             void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
+    return rmsnorm_bwd(route, views, sr, dy, nullptr, r_prime, rstd, g, dres, rows, cols, sr_seed, sr_offset, dr,
+                       dr_row, dr_col, workspace, workspace_bytes, stream);
+}
+
+int fp4_residual_rmsnorm_bwd_parts(int route, unsigned views, int sr, const void* dy, const float* part,
+                                   const void* r_prime, const float* rstd, const void* g, const void* dres,
+                                   int64_t rows, int64_t cols, uint64_t sr_seed, uint64_t sr_offset, void* dr,
+                                   fp4_tensor* dr_row, fp4_tensor* dr_col, void* workspace, size_t workspace_bytes,
+                                   fp4_stream_t stream) {
+    if (!part && rows > 0 && cols > 0) return FP4_ERR_INVALID_ARG;
+    return rmsnorm_bwd(route, views, sr, dy, part, r_prime, rstd, g, dres, rows, cols, sr_seed, sr_offset, dr,
+                       dr_row, dr_col, workspace, workspace_bytes, stream);
+}
+
+// The adjacent RMSNorm backward's row terms, computed in a plain bf16 store
+// epilogue (see fp4_linear_dgrad_rmsnorm).
+struct RmsTerms {
+    const void* r_prime;
+    const float* rstd;
+    const void* g;
+    float* part;
+};
+
+static int linear(const fp4_tensor* a, const fp4_tensor* b, void* c, int out_dtype, float beta, fp4_stream_t stream,
+                  const RmsTerms* rms = nullptr) {
     if (!a || !b || !c) return FP4_ERR_INVALID_ARG;
     if (out_dtype != FP4_OUT_F32 && out_dtype != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;
     if (!route_ok(a->route) || !route_ok(b->route)) return FP4_ERR_INVALID_ARG;
@@ -265,6 +296,12 @@ static int linear(const fp4_tensor* a, const fp4_tensor* b, void* c, int out_dty
     g.c = c;
     g.out_dtype = out_dtype;
     g.beta = beta;
+    if (rms) {
+        g.rms_rp = static_cast<const uint16_t*>(rms->r_prime);
+        g.rms_g = static_cast<const uint16_t*>(rms->g);
+        g.rms_rstd = rms->rstd;
+        g.rms_part = rms->part;
+    }
     return launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -451,6 +488,15 @@ int fp4_linear_fprop(const fp4_tensor* x_row, const fp4_tensor* w_row, void* y, 
 int fp4_linear_dgrad(const fp4_tensor* dy_row, const fp4_tensor* w_col, void* dx, int out_dtype, float beta,
                      fp4_stream_t stream) {
     return linear(dy_row, w_col, dx, out_dtype, beta, stream);
+}
+
+int fp4_linear_dgrad_rmsnorm(const fp4_tensor* dy_row, const fp4_tensor* w_col, void* dx, const void* r_prime,
+                             const float* rstd, const void* g, float* part, fp4_stream_t stream) {
+    if (!r_prime || !rstd || !g || !part || !aligned16(r_prime) || !aligned16(g) ||
+        (reinterpret_cast<uintptr_t>(rstd) & 3u) || (reinterpret_cast<uintptr_t>(part) & 3u))
+        return FP4_ERR_INVALID_ARG;
+    const RmsTerms rms{r_prime, rstd, g, part};
+    return linear(dy_row, w_col, dx, FP4_OUT_BF16, 0.0f, stream, &rms);
 }
 
 int fp4_linear_wgrad(const fp4_tensor* dy_col, const fp4_tensor* x_col, float* dw, float beta, fp4_stream_t stream) {

@@ -94,7 +94,25 @@ __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_bwd_stats_kernel(const ui
     if (threadIdx.x == 0) mean_g[row] = tot / (float)C;
 }
 
+// One thread per row: the row terms that a data-gradient epilogue wrote per
+// 64-column block, summed in block order, divided by the row length.
+__global__ void __launch_bounds__(256) rms_parts_reduce_kernel(const float* __restrict__ part, int64_t R,
+                                                               int64_t nparts, int64_t C, float* __restrict__ mean_g) {
+    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= R) return;
+    const float* pr = part + row * nparts;
+    float s = 0.0f;
+    for (int64_t j = 0; j < nparts; ++j) s = __fadd_rn(s, pr[j]);
+    mean_g[row] = s / (float)C;
+}
+
 }  // namespace
+
+int launch_rms_parts_reduce(const float* part, int64_t R, int64_t nparts, int64_t C, float* mean_g,
+                            cudaStream_t stream) {
+    rms_parts_reduce_kernel<<<(unsigned)((R + 255) / 256), 256, 0, stream>>>(part, R, nparts, C, mean_g);
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
 
 int launch_rmsnorm_fwd_stats(const uint16_t* r, const uint16_t* b, int64_t R, int64_t C, int64_t ld, float eps,
                              uint16_t* r_out, float* rstd, cudaStream_t stream) {

@@ -466,7 +466,11 @@ FP4_DEV void store_bf16x32(uint16_t* dst, const float* v) {
 }
 
 // ----------------------------------------------------------------- kernel -
-enum { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_QKV_ROPE = 3 };
+// EPI_STORE_RMS: the plain store (bf16) that also writes the adjacent
+// RMSNorm backward's row terms (a separate instantiation, so that the plain
+// store's register allocation is untouched)
+enum { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_QKV_ROPE = 3, EPI_STORE_RMS = 4 };
+__host__ __device__ constexpr bool is_store(int epi) { return epi == EPI_STORE || epi == EPI_STORE_RMS; }
 
 struct KParams {
     const uint8_t* a_scales;
@@ -498,6 +502,11 @@ struct KParams {
     const float* rope_sin;
     int64_t seq_len;
     int heads_q, heads_kv;
+    // plain bf16 store: the adjacent RMSNorm backward's row terms
+    const uint16_t* rms_rp;
+    const uint16_t* rms_g;
+    const float* rms_rstd;
+    float* rms_part;
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -531,9 +540,9 @@ struct Cfg {
     static constexpr int OUT_ROW = fit(EPI_WARPS * 4096) >= MAX_STAGES_OUT ? 128 : 64;  // bytes per box row
     static constexpr int OUT_BOX = 32 * OUT_ROW;
     static constexpr int OUT_BUFS =
-        EPI != EPI_STORE ? 0 : (fit(EPI_WARPS * 2 * OUT_BOX) >= MAX_STAGES_OUT ? 2 : 1);
+        !is_store(EPI) ? 0 : (fit(EPI_WARPS * 2 * OUT_BOX) >= MAX_STAGES_OUT ? 2 : 1);
     static constexpr int STAGING =
-        EPI == EPI_STORE      ? EPI_WARPS * OUT_BUFS * OUT_BOX
+        is_store(EPI)         ? EPI_WARPS * OUT_BUFS * OUT_BOX
         : EPI == EPI_QKV_ROPE ? 0
                               : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
     static constexpr int STAGES = fit(STAGING);
@@ -880,10 +889,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const int64_t m = m0 + lr;
             const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-            if constexpr (EPI == EPI_STORE) {
+            if constexpr (is_store(EPI)) {
                 constexpr int NC = BN / 64;  // 32-column chunks per thread
                 uint32_t r[NC * 32];
-#pragma unroll
                 if constexpr (NC == 4)
                     tmem_ld128(lane_base + half * (BN / 2), r);
                 else
@@ -892,6 +900,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 release_acc();
                 float sa = 1.0f;
                 if (NV) sa = __fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]);
+                // EPI_STORE_RMS (bf16 only): the consumer is a residual-RMSNorm
+                // backward, whose row mean needs sum_n fl32(dy * g) *
+                // fl32(r' * rstd) over the bf16 values this store writes.  Each
+                // thread adds its row's terms box by box, in column order, and
+                // writes one binary32 partial per 64-column block (no atomics:
+                // the blocks are summed in a fixed order later).
+                float rms_acc = 0.0f, rms_rs = 0.0f;
+                if constexpr (EPI == EPI_STORE_RMS) rms_rs = p.rms_rstd[m];
                 const bool tma_out = p.beta == 0.0f || p.beta == 1.0f;
                 if (tma_out) {
                     // rows [32q, 32q+32) of the tile through this warp's
@@ -928,6 +944,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 w[i] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * WORDS * bi + 2 * i]) * alpha) |
                                        ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * WORDS * bi + 2 * i + 1]) * alpha)
                                         << 16);
+                            if constexpr (EPI == EPI_STORE_RMS) {
+                                const uint16_t* xr = p.rms_rp + m * p.N + n;
+                                const uint16_t* gr = p.rms_g + n;
+#pragma unroll
+                                for (int c8 = 0; c8 < WORDS / 4; ++c8) {  // 8 columns per 16-byte load
+                                    const uint4 xv = *reinterpret_cast<const uint4*>(xr + 8 * c8);
+                                    const uint4 gv = *reinterpret_cast<const uint4*>(gr + 8 * c8);
+                                    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, gs[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k) {
+                                        const uint32_t dw = w[4 * c8 + k];
+                                        rms_acc = fmaf(__fmul_rn(bf16_lo(dw), bf16_lo(gs[k])),
+                                                       __fmul_rn(bf16_lo(xs[k]), rms_rs), rms_acc);
+                                        rms_acc = fmaf(__fmul_rn(bf16_hi(dw), bf16_hi(gs[k])),
+                                                       __fmul_rn(bf16_hi(xs[k]), rms_rs), rms_acc);
+                                    }
+                                }
+                                if (((bi + 1) * 2 * WORDS) % 64 == 0) {  // a 64-column block is complete
+                                    p.rms_part[m * (p.N >> 6) + ((n + 2 * WORDS - 64) >> 6)] = rms_acc;
+                                    rms_acc = 0.0f;
+                                }
+                            }
                         }
                         // this lane's row: 16-byte chunk k lands at k ^ (row & 7)
                         // (128B swizzle) or k ^ ((row >> 1) & 3) (64B swizzle)
@@ -986,7 +1024,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t pk[64];  // bf16x2 of the head's 128 values
                 {
                     uint32_t r[128];
-#pragma unroll
                     tmem_ld128(lane_base + 128 * half, r);
                     tc_fence_before();
                     release_acc();
@@ -1128,7 +1165,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t dp[32];  // bf16x2 of dh (64 columns)
                 {
                     uint32_t r[64];
-#pragma unroll
                     tmem_ld64(lane_base + 64 * half, r);
                     tc_fence_before();
                     release_acc();
@@ -1233,7 +1269,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             acc_phase ^= 1;
         }
     }
-    if (EPI == EPI_STORE && warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores done with shared memory
+    if (is_store(EPI) && warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores done with shared memory
     tc_fence_before();
     __syncthreads();
     if (CM > 1) cluster_sync();  // no peer still multicasts into this CTA
@@ -1334,7 +1370,7 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
             !make_sf_map(&tsb, g.b_scales, (g.b_rows / 128) * k_atoms, C::SF_CHUNKS))
             return FP4_ERR_CUDA;
     }
-    if (EPI == EPI_STORE && (g.beta == 0.0f || g.beta == 1.0f) && !make_out_map(&tc, g.c, g.M, g.N, g.out_dtype, C::OUT_ROW))
+    if (is_store(EPI) && (g.beta == 0.0f || g.beta == 1.0f) && !make_out_map(&tc, g.c, g.M, g.N, g.out_dtype, C::OUT_ROW))
         return FP4_ERR_CUDA;
     auto kern = fp4_gemm_kernel<NV, BN, EPI, CM, P2>;
     int dev = 0;
@@ -1405,6 +1441,10 @@ KParams kparams_of(const GemmParams& g) {
     p.seq_len = g.seq_len;
     p.heads_q = g.heads_q;
     p.heads_kv = g.heads_kv;
+    p.rms_rp = g.rms_rp;
+    p.rms_g = g.rms_g;
+    p.rms_rstd = g.rms_rstd;
+    p.rms_part = g.rms_part;
     return p;
 }
 
@@ -1440,6 +1480,13 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     }
     const bool wide = (g.N % 256) == 0;
     const int64_t units_1 = (g.M / BM) * (g.N / (wide ? 256 : 128));
+    if (g.rms_part) {  // bf16 store + RMSNorm row terms: the pair kernel, else 128-wide single CTAs
+        const int64_t units_128 = (g.M / BM) * (g.N / 128);
+        if (g.nv) return wide && pair ? launch_t<true, 256, EPI_STORE_RMS, 2, true>(g, kp, units_1 / 2, stream)
+                                      : launch_t<true, 128, EPI_STORE_RMS, 1>(g, kp, units_128, stream);
+        return wide && pair ? launch_t<false, 256, EPI_STORE_RMS, 2, true>(g, kp, units_1 / 2, stream)
+                            : launch_t<false, 128, EPI_STORE_RMS, 1>(g, kp, units_128, stream);
+    }
     if (g.nv) {
         // 256-wide tiles go to the CTA-pair kernel for both formats; with the
         // scale copies off the MMA thread, NVFP4's twice-as-many copies no

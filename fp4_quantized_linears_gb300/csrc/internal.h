@@ -52,6 +52,9 @@ int launch_rmsnorm_fwd_stats(const uint16_t* r, const uint16_t* b, int64_t R, in
                              uint16_t* r_out, float* rstd, cudaStream_t stream);
 int launch_rmsnorm_bwd_stats(const uint16_t* dy, const uint16_t* rp, const float* rstd, const uint16_t* g, int64_t R,
                              int64_t C, float* mean_g, cudaStream_t stream);
+// mean_g[row] = (sum over j in order of part[row][j]) / C
+int launch_rms_parts_reduce(const float* part, int64_t R, int64_t nparts, int64_t C, float* mean_g,
+                            cudaStream_t stream);
 
 int launch_quantize(const QuantParams& p, cudaStream_t stream);
 // amax slots (4 bytes each) a quantizer call needs in its workspace
@@ -95,6 +98,12 @@ struct GemmParams {
     const float* rope_sin;
     int64_t seq_len;
     int heads_q, heads_kv;
+    // plain bf16 store feeding a residual-RMSNorm backward: the row terms
+    // part[m][n / 64] = sum over the 64-column block of fl32(c * g) * fl32(r' * rstd)
+    const uint16_t* rms_rp;  // r' bf16 [M][N]
+    const uint16_t* rms_g;   // g bf16 [N]
+    const float* rms_rstd;   // [M]
+    float* rms_part;         // [M][N / 64], or NULL
 };
 
 int launch_gemm(const GemmParams& p, cudaStream_t stream);

@@ -17,7 +17,9 @@ gradient only; no Hadamard.  Each block is
 and the backward runs the same boundaries in reverse: the residual-RMSNorm
 backward producer emits the residual gradient together with its FP4 views,
 which are the output-gradient operands of the preceding linear; the SwiGLU
-backward producer fuses the W2 data gradient with the SiLU derivative.
+backward producer fuses the W2 data gradient with the SiLU derivative; the
+data-gradient contractions that feed an RMSNorm backward (W1/W3 and QKV)
+also emit that backward's row terms, so it never re-reads their output.
 
 Only argument marshalling happens here: every step is a call into
 libfp4lin.  Buffers are allocated once by the constructor (torch device
@@ -30,9 +32,9 @@ from dataclasses import dataclass, field
 import torch
 
 from . import (FP4_FLAG_SR_ROW, FP4_FLAG_WEIGHT_2D, FP4_OUT_BF16, FP4_VIEW_COL, FP4_VIEW_ROW, alloc_view,
-               fp4_linear_dgrad, fp4_linear_fprop, fp4_linear_wgrad, fp4_quantize, fp4_quantize_workspace_bytes,
-               fp4_residual_rmsnorm_bwd, fp4_residual_rmsnorm_fwd, fp4_rmsnorm_bwd_workspace_bytes,
-               fp4_swiglu_bwd, fp4_swiglu_fwd)
+               fp4_linear_dgrad, fp4_linear_dgrad_rmsnorm, fp4_linear_fprop, fp4_linear_wgrad, fp4_quantize,
+               fp4_quantize_workspace_bytes, fp4_residual_rmsnorm_bwd_parts, fp4_residual_rmsnorm_fwd,
+               fp4_rmsnorm_bwd_workspace_bytes, fp4_swiglu_bwd, fp4_swiglu_fwd)
 
 
 @dataclass
@@ -112,6 +114,7 @@ class FP4LinearStack:
         self.dqkv = torch.zeros((T, q), **bf)        # attention stand-in gradient (K, V parts stay 0)
         self.dattn = torch.empty((T, d), **bf)
         self.dy = torch.empty((T, d), **bf)
+        self.part = torch.empty((T, d // 64), dtype=torch.float32, device=dev)  # RMSNorm row terms
         self.dr2 = torch.empty((T, d), **bf)                            # gradient of r2
         self.dr1 = [torch.empty((T, d), **bf) for _ in range(2)]        # gradient of r1, alternating
         self.gviews = {}
@@ -174,12 +177,14 @@ class FP4LinearStack:
                 fp4_swiglu_bwd(dF[0], wv["w2"][1], f, s["a1"], s["a3"], da13_tap=self.da13, quantize=False)
                 fp4_quantize(self.da13, r, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=off + 1,
                              row_out=gv["da13"][0], col_out=gv["da13"][1], workspace=self.ws)
-            fp4_linear_dgrad(gv["da13"][0], wv["w13"][1], self.dy, FP4_OUT_BF16)
+            fp4_linear_dgrad_rmsnorm(gv["da13"][0], wv["w13"][1], s["r2"], s["rstd2"], self.g2, dx=self.dy,
+                                     part=self.part)
             fp4_linear_wgrad(gv["da13"][1], s["y2"][1], dw["w13"])
             # residual-RMSNorm backward -> gradient of r2 and its views (the O projection's dY)
             dr2 = self.dr2
-            fp4_residual_rmsnorm_bwd(self.dy, s["r2"], s["rstd2"], self.g2, dh_out, r, 3, True, sr_seed, off + 2,
-                                     dr=dr2, dr_row=gv["dr2"][0], dr_col=gv["dr2"][1], workspace=self.ws)
+            fp4_residual_rmsnorm_bwd_parts(self.dy, self.part, s["r2"], s["rstd2"], self.g2, dh_out, r, 3, True,
+                                           sr_seed, off + 2, dr=dr2, dr_row=gv["dr2"][0], dr_col=gv["dr2"][1],
+                                           workspace=self.ws)
             fp4_linear_wgrad(gv["dr2"][1], s["attn"][1], dw["o"])
             fp4_linear_dgrad(gv["dr2"][0], wv["o"][1], self.dattn, FP4_OUT_BF16)
             # attention stand-in backward: dQKV = [dattn | 0 | 0]
@@ -187,15 +192,16 @@ class FP4LinearStack:
             fp4_quantize(self.dqkv, r, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=off + 3, row_out=gv["dqkv"][0],
                          col_out=gv["dqkv"][1], workspace=self.ws)
             fp4_linear_wgrad(gv["dqkv"][1], s["y1"][1], dw["qkv"])
-            fp4_linear_dgrad(gv["dqkv"][0], wv["qkv"][1], self.dy, FP4_OUT_BF16)
+            fp4_linear_dgrad_rmsnorm(gv["dqkv"][0], wv["qkv"][1], s["r1"], s["rstd1"], self.g1, dx=self.dy,
+                                     part=self.part)
             # residual-RMSNorm backward -> gradient of the block input, quantized
             # for the preceding block's FFN (in that block's route)
             prev_route = self.blocks[i - 1].route if i > 0 else r
             dF = self.gviews[prev_route]["dF"] if i > 0 else self.views_in[r]
             dr1 = self.dr1[i % 2]  # never the buffer that holds dh_out (block i + 1's)
-            fp4_residual_rmsnorm_bwd(self.dy, s["r1"], s["rstd1"], self.g1, dr2, prev_route,
-                                     3 if i > 0 else FP4_VIEW_ROW, True, sr_seed, off + 4, dr=dr1, dr_row=dF[0],
-                                     dr_col=dF[1] if i > 0 else None, workspace=self.ws)
+            fp4_residual_rmsnorm_bwd_parts(self.dy, self.part, s["r1"], s["rstd1"], self.g1, dr2, prev_route,
+                                           3 if i > 0 else FP4_VIEW_ROW, True, sr_seed, off + 4, dr=dr1,
+                                           dr_row=dF[0], dr_col=dF[1] if i > 0 else None, workspace=self.ws)
             dh_out = dr1
         return dh_out
 

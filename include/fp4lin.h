@@ -4,11 +4,13 @@
  * sm_103a (GB300).
  *
  * Two halves, as in the paper's boundary contract (Sec. 3.1):
- *   producers  fp4_quantize(_hybrid), fp4_swiglu_fwd/bwd, fp4_residual_rmsnorm_fwd/bwd,
+ *   producers  fp4_quantize(_hybrid), fp4_swiglu_fwd/bwd, fp4_residual_rmsnorm_fwd/bwd(_parts),
  *              fp4_qkv_rope_fwd/bwd turn BF16 tensors into E2M1 codes plus
  *              scales (or the BF16 attention inputs) in the physical
  *              layout the next contraction consumes;
- *   consumers  fp4_linear_fprop/dgrad/wgrad, block-scaled tcgen05 GEMMs.
+ *   consumers  fp4_linear_fprop/dgrad/wgrad (and fp4_linear_dgrad_rmsnorm,
+ *              a Dgrad that also emits the next RMSNorm backward's row
+ *              terms), block-scaled tcgen05 GEMMs.
  *
  * General conventions
  *  - Every pointer named "device" is caller-owned CUDA device memory.  The
@@ -339,6 +341,35 @@ FP4_API int fp4_residual_rmsnorm_bwd(int route, unsigned views, int sr, const vo
                                      uint64_t sr_seed, uint64_t sr_offset, void* dr, fp4_tensor* dr_row,
                                      fp4_tensor* dr_col, void* workspace, size_t workspace_bytes,
                                      fp4_stream_t stream);
+
+/* Data-gradient contraction whose consumer is a residual-RMSNorm backward
+ * (Sec. 3.2: the backward combines QKV gradient production with the adjacent
+ * RMSNorm reduction when their data dependencies align).  Computes
+ * dx = dY . W exactly as fp4_linear_dgrad(dy_row, w_col, dx, FP4_OUT_BF16, 0)
+ * and, in the same epilogue, for every row m and 64-column block j of dx,
+ *   part[m][j] = sum over the block's columns n, in increasing order, of
+ *                fl32(dx[m][n] * g[n]) * fl32(r'[m][n] * rstd[m])
+ * (binary32, fused multiply-add accumulation), the terms of the RMSNorm
+ * backward's row mean over the bf16 values written to dx.
+ * r_prime: device bf16 [rows][cols] (the forward's retained r'), rstd: device
+ * binary32 [rows], g: device bf16 [cols], part: device binary32
+ * [rows][cols / 64] written by the call (rows = dy_row->rows, cols =
+ * w_col->rows); r_prime and g 16-byte aligned.  Errors as fp4_linear_dgrad,
+ * FP4_ERR_INVALID_ARG for a missing or misaligned pointer. */
+FP4_API int fp4_linear_dgrad_rmsnorm(const fp4_tensor* dy_row, const fp4_tensor* w_col, void* dx, const void* r_prime,
+                                     const float* rstd, const void* g, float* part, fp4_stream_t stream);
+
+/* fp4_residual_rmsnorm_bwd with the row means taken from the partial sums
+ * that fp4_linear_dgrad_rmsnorm wrote for this dy:
+ *   mean_g[m] = (sum over j = 0 .. cols/64 - 1, in order, of part[m][j]) / cols
+ * instead of a second pass over dy; everything else as
+ * fp4_residual_rmsnorm_bwd (same workspace).  part: device binary32
+ * [rows][cols / 64]. */
+FP4_API int fp4_residual_rmsnorm_bwd_parts(int route, unsigned views, int sr, const void* dy, const float* part,
+                                           const void* r_prime, const float* rstd, const void* g, const void* dres,
+                                           int64_t rows, int64_t cols, uint64_t sr_seed, uint64_t sr_offset,
+                                           void* dr, fp4_tensor* dr_row, fp4_tensor* dr_col, void* workspace,
+                                           size_t workspace_bytes, fp4_stream_t stream);
 
 /* Workspace of fp4_residual_rmsnorm_bwd: rows * 4 bytes of row statistics
  * plus the quantizer's workspace, rounded up to 256 bytes.  Host only. */
