@@ -20,7 +20,7 @@
 //                   FP4 views of [da1 | da3] for the W1/W3 Dgrad (row view,
 //                   stochastic rounding) and Wgrad (column view).
 //
-// Structure: a persistent kernel, one CTA per SM (352 threads), clusters of
+// Structure: a persistent kernel, one CTA per SM (384 threads), clusters of
 // CM CTAs along M that share the B tile through TMA multicast:
 //   warp 0      TMA producer: A tile (128 rows), this CTA's share of the B
 //               tile multicast to the cluster, scale atoms (1D bulk copies),
@@ -29,9 +29,10 @@
 //               MMAs (kind::mxf4 E8M0 / kind::mxf4nvf4 E4M3) into a
 //               128 x BN FP32 accumulator; the stage is released to every
 //               CTA of the cluster by a multicast tcgen05.commit;
-//   warp 10     one thread copies each landed stage's scale atoms into TMEM
-//               (tcgen05.cp 32x128b.warpx4) ahead of the MMA thread, which
-//               waits for the copies' commit instead of the landing;
+//   warps 10-11 one thread each copies half of each landed stage's scale
+//               atoms into TMEM (tcgen05.cp 32x128b.warpx4) ahead of the MMA
+//               thread, which waits for both copies' commits instead of the
+//               landing;
 //   warps 2-9   epilogue: drain the accumulator from TMEM into registers
 //               (each warp one lane quarter x one column half), release it so
 //               the next tile's MMAs start, then finish the tile while the
@@ -65,8 +66,9 @@ constexpr int BK_BYTES = BK / 2;
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
 constexpr int MAX_STAGES = 8;
 constexpr int EPI_WARPS = 8;
-constexpr int SF_WARP = 2 + EPI_WARPS;  // the warp that moves scale factors into TMEM
-constexpr int THREADS = 32 * (SF_WARP + 1);
+constexpr int SF_WARP = 2 + EPI_WARPS;  // the first of the warps that move scale factors into TMEM
+constexpr int SF_WARPS = 2;             // each copies every SF_WARPS-th scale chunk of a stage
+constexpr int THREADS = 32 * (SF_WARP + SF_WARPS);
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;  // first TMEM column of the scale-factor region
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
@@ -617,9 +619,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], P2 ? 1 : CM);  // pair: the leader's commit reaches each CTA once
-            mbar_init(&sf_full[s], 1);
+            mbar_init(&sf_full[s], SF_WARPS);
         }
-        mbar_init(sf_drain, 1);
+        mbar_init(sf_drain, SF_WARPS);
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, P2 ? 2 * EPI_WARPS : EPI_WARPS);  // pair: both CTAs' epilogues, on the leader
         mbar_init(drain_bar, 1);
@@ -799,7 +801,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // epilogue wait on acc_full can see an extra phase)
         tc_commit<G>(drain_bar);
         mbar_wait(drain_bar, 0);
-    } else if (warp == SF_WARP && lane == 0 && (!P2 || rank == 0)) {
+    } else if (warp >= SF_WARP && lane == 0 && (!P2 || rank == 0)) {
         // ------------------------------------------------ scale factors ---
         // Each landed stage's scale atoms go to that stage's TMEM columns
         // (replicated into the four lane quarters), issued from this thread
@@ -809,6 +811,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // again once the stage lands anew: the producer refills it only after
         // the MMAs that read the previous copies have completed.
         // (pair: the leader copies for both CTAs, each from its own stage)
+        // Two such threads, in two warps, share each stage's chunks: one
+        // thread's copies (12 per stage for NVFP4) took about as long as the
+        // stage's MMAs.  Both commit to sf_full (arrival count SF_WARPS).
+        const int sfi = warp - SF_WARP;
         const uint32_t sf_base = tmem + SF_COL0;
         int stage = 0;
         uint32_t phase = 0;
@@ -824,7 +830,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t sfa_col = sf_base + stage * C::SF_COLS;
                 const uint32_t sfb_col = sfa_col + C::SF_COLS_A;
 #pragma unroll
-                for (int c = 0; c < C::SF_CHUNKS; ++c) {
+                for (int c = sfi; c < C::SF_CHUNKS; c += SF_WARPS) {
                     tc_cp_sf<G>(sfa_col + 4 * c,
                                 smem_desc(smem_u32(stage_sfa(stage) + c * 512), 0, 128, LAYOUT_NONE));
 #pragma unroll
