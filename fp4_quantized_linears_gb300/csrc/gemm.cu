@@ -1141,17 +1141,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                     epi_sync();
                     if (!epi_ok) break;
                     // column-facing view: stored row = output column, blocks along the tokens
-#pragma unroll 1
-                    for (int k = 0; k < 2; ++k) {
-                        const int idx = et + 256 * k, j = idx >> 7, cidx = idx & 127;
-                        float v[32];
+                    // column pairs: one 32-bit load per two values
+                    {
+                        const int j = et >> 6, cp = et & 63;
+                        uint32_t w[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = bf16_to_f32(hs[(32 * j + i) * ST_LDS + cidx]);
-                        uint4 pk;
-                        uint32_t sc = mx_block_rn(v, pk);
-                        *reinterpret_cast<uint4*>(p.q_col_codes + (n0 + cidx) * (p.M >> 1) + ((m0 + 32 * j) >> 1)) =
-                            pk;
-                        col_atom[atom_off(cidx, j)] = (uint8_t)sc;
+                        for (int i = 0; i < 32; ++i)
+                            w[i] = *reinterpret_cast<const uint32_t*>(&hs[(32 * j + i) * ST_LDS + 2 * cp]);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int cidx = 2 * cp + h;
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
+                            uint4 pk;
+                            uint32_t sc = mx_block_rn(v, pk);
+                            *reinterpret_cast<uint4*>(p.q_col_codes + (n0 + cidx) * (p.M >> 1) +
+                                                      ((m0 + 32 * j) >> 1)) = pk;
+                            col_atom[atom_off(cidx, j)] = (uint8_t)sc;
+                        }
                     }
                     epi_sync();
                     if (!epi_ok) break;
@@ -1244,18 +1252,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (p.quantize) {
                     epi_sync();
                     if (!epi_ok) break;
+                    // column pairs: each thread reads 32 bf16x2 words down a pair of
+                    // columns (one 32-bit load per two values) and encodes both
 #pragma unroll 1
-                    for (int k = 0; k < 4; ++k) {
-                        const int idx = et + 256 * k, which = idx >> 9, j = (idx >> 7) & 3, cidx = idx & 127;
+                    for (int k = 0; k < 2; ++k) {
+                        const int idx = et + 256 * k, which = idx >> 8, j = (idx >> 6) & 3, cp = idx & 63;
                         const uint16_t* src = which ? s3 : s1;
-                        float v[32];
+                        uint32_t w[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = bf16_to_f32(src[(32 * j + i) * ST_LDS + cidx]);
-                        uint4 pk;
-                        uint32_t sc = mx_block_rn(v, pk);
-                        const int64_t srow = (which ? p.f : 0) + n0 + cidx;
-                        *reinterpret_cast<uint4*>(p.q_col_codes + srow * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pk;
-                        atoms[1024 + which * 512 + atom_off(cidx, j)] = (uint8_t)sc;
+                        for (int i = 0; i < 32; ++i)
+                            w[i] = *reinterpret_cast<const uint32_t*>(&src[(32 * j + i) * ST_LDS + 2 * cp]);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int cidx = 2 * cp + h;
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
+                            uint4 pk;
+                            uint32_t sc = mx_block_rn(v, pk);
+                            const int64_t srow = (which ? p.f : 0) + n0 + cidx;
+                            *reinterpret_cast<uint4*>(p.q_col_codes + srow * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pk;
+                            atoms[1024 + which * 512 + atom_off(cidx, j)] = (uint8_t)sc;
+                        }
                     }
                     epi_sync();
                     if (!epi_ok) break;
