@@ -96,3 +96,30 @@ def test_gemm_validation_codes():
 def test_status_strings():
     assert F.status_string(0) == "ok"
     assert F.status_string(F.FP4_ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_dgrad_rmsnorm_validation_codes():
+    """The Dgrad that emits RMSNorm row terms and the RMSNorm backward that
+    consumes them reject missing or misaligned pointers and mismatched
+    routes on the host."""
+    L = F.load()
+    dy, w = _t(128, 256), _t(256, 256)
+    c, ok16, f4 = ctypes.c_void_p(16), ctypes.c_void_p(32), ctypes.c_void_p(64)
+    d = L.fp4_linear_dgrad_rmsnorm
+    assert d(ctypes.byref(dy), ctypes.byref(w), c, None, f4, ok16, f4, None) == F.FP4_ERR_INVALID_ARG   # no r'
+    assert d(ctypes.byref(dy), ctypes.byref(w), c, ok16, None, ok16, f4, None) == F.FP4_ERR_INVALID_ARG  # no rstd
+    assert d(ctypes.byref(dy), ctypes.byref(w), c, ok16, f4, None, f4, None) == F.FP4_ERR_INVALID_ARG    # no g
+    assert d(ctypes.byref(dy), ctypes.byref(w), c, ok16, f4, ok16, None, None) == F.FP4_ERR_INVALID_ARG  # no terms
+    assert d(ctypes.byref(dy), ctypes.byref(w), c, ctypes.c_void_p(18), f4, ok16, f4, None) == F.FP4_ERR_INVALID_ARG
+    assert d(ctypes.byref(dy), ctypes.byref(w), c, ok16, f4, ctypes.c_void_p(40), f4, None) == F.FP4_ERR_INVALID_ARG
+    assert d(ctypes.byref(dy), ctypes.byref(w), c, ok16, ctypes.c_void_p(66), ok16, f4, None) == F.FP4_ERR_INVALID_ARG
+    wn = _t(256, 256, route=1, oc=1)
+    assert d(ctypes.byref(dy), ctypes.byref(wn), c, ok16, f4, ok16, f4, None) == F.FP4_ERR_ROUTE_MISMATCH
+    r = L.fp4_residual_rmsnorm_bwd_parts
+    t = _t()
+    # row terms missing
+    assert r(0, 3, 1, ok16, None, ok16, f4, ok16, None, 128, 128, 0, 0, ok16, ctypes.byref(t), ctypes.byref(t), ok16,
+             1 << 20, None) == F.FP4_ERR_INVALID_ARG
+    # shape rule of the RMSNorm backward
+    assert r(0, 3, 1, ok16, f4, ok16, f4, ok16, None, 100, 128, 0, 0, ok16, ctypes.byref(t), ctypes.byref(t), ok16,
+             1 << 20, None) == F.FP4_ERR_UNSUPPORTED_SHAPE
