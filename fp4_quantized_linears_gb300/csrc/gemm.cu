@@ -20,15 +20,17 @@
 //                   FP4 views of [da1 | da3] for the W1/W3 Dgrad (row view,
 //                   stochastic rounding) and Wgrad (column view).
 //
-// Structure: a persistent kernel, one CTA per SM (384 threads), clusters of
-// CM CTAs along M that share the B tile through TMA multicast:
+// Structure: a persistent kernel, one CTA per SM (384 threads); with an even
+// number of 128-row M blocks, CTA pairs (cta_group::2) share one M = 256 MMA
+// whose B tile is split between the two CTAs by N halves:
 //   warp 0      TMA producer: A tile (128 rows), this CTA's share of the B
-//               tile multicast to the cluster, scale atoms (1D bulk copies),
-//               into a STAGES-deep ring of mbarrier-guarded stages;
+//               tile, scale atoms, into a STAGES-deep ring of
+//               mbarrier-guarded stages (pair: every load of both CTAs
+//               completes on the pair leader's barrier);
 //   warp 1      owns the TMEM allocation; one thread issues the block-scaled
 //               MMAs (kind::mxf4 E8M0 / kind::mxf4nvf4 E4M3) into a
-//               128 x BN FP32 accumulator; the stage is released to every
-//               CTA of the cluster by a multicast tcgen05.commit;
+//               128 x BN FP32 accumulator per CTA; its commits release the
+//               stage in both CTAs of a pair;
 //   warps 10-11 one thread each copies half of each landed stage's scale
 //               atoms into TMEM (tcgen05.cp 32x128b.warpx4) ahead of the MMA
 //               thread, which waits for both copies' commits instead of the
@@ -40,6 +42,8 @@
 //               swizzled 32-row shared buffer per warp and a TMA
 //               tensor store (or TMA reduce-add for beta = 1), so every
 //               global write is a bulk transfer of whole 32-byte sectors.
+// Every operand load brings data into the issuing CTA's own shared memory;
+// no load is multicast across the cluster.
 // Every mbarrier wait is bounded: a wait that runs out sets the sticky status
 // word to FP4_ERR_TIMEOUT, the roles drain what they issued and the CTA
 // returns, releasing its tensor memory.
@@ -127,15 +131,6 @@ FP4_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64
         "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
-// The same box delivered to the same offset in every CTA of `mask`, each
-// completing bytes on its own barrier at the same offset.
-FP4_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
 FP4_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -200,21 +195,14 @@ FP4_DEV void tc_commit(uint64_t* bar) {
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                      : "memory");
 }
-// arrive on the barrier at the same offset in every CTA of `mask`
-template <int G = 1>
-FP4_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-    if (G == 2)
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                smem_u32(bar)),
-            "h"(mask)
-            : "memory");
-    else
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                smem_u32(bar)),
-            "h"(mask)
-            : "memory");
+// tcgen05.commit of the pair leader: the arrive reaches the barrier at the
+// same offset in both CTAs of the pair (`mask` = 3)
+FP4_DEV void tc_commit_pair(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 // shared-memory matrix descriptor (tcgen05): start, LBO, SBO (bytes >> 4),
@@ -561,7 +549,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
                     const __grid_constant__ CUtensorMap tmSB, KParams p) {
     using C = Cfg<NV, BN, EPI, P2>;
-    static_assert(!P2 || (CM == 2 && BN == 256 && EPI != EPI_SWIGLU_BWD), "pair mode: 256-wide tiles");
+    static_assert(P2 ? CM == 2 : CM == 1, "clusters are CTA pairs");
+    static_assert(!P2 || BN == 256 || EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD, "pair tile widths");
     constexpr int G = P2 ? 2 : 1;       // tcgen05 CTA group
     constexpr int MMA_M = P2 ? 2 * BM : BM;
     constexpr int STAGES = C::STAGES;
@@ -618,7 +607,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], P2 ? 1 : CM);  // pair: the leader's commit reaches each CTA once
+            mbar_init(&empty[s], 1);  // pair: the leader's commit reaches each CTA once
             mbar_init(&sf_full[s], SF_WARPS);
         }
         mbar_init(sf_drain, SF_WARPS);
@@ -655,7 +644,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CM > 1) cluster_sync();  // peers' barriers are initialised before any multicast
+    if (CM > 1) cluster_sync();  // the peer's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -681,7 +670,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t fb = mapa_rank(smem_u32(&full[stage]), 0);
                     if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::TX_BYTES);
                     tma_load_2d_pair(stage_a(stage), &tmA, kb * BK_BYTES, (int)m0, fb);
-                    tma_load_2d_pair(stage_b(stage), &tmB, kb * BK_BYTES, (int)b_row(n0, (int)rank), fb);
+                    // B rows of this CTA's N-half: 128 rows of W1 / W3 (SwiGLU
+                    // forward), else rows [n0 + rank * BN/2, + BN/2)
+                    const int64_t brow = EPI == EPI_SWIGLU_FWD ? b_row(n0, (int)rank) : n0 + (int64_t)rank * (BN / 2);
+                    tma_load_2d_pair(stage_b(stage), &tmB, kb * BK_BYTES, (int)brow, fb);
                     tma_load_2d_pair(stage_sfa(stage), &tmSA, 0, (int)((m0 >> 7) * k_atoms + kb * C::SF_CHUNKS), fb);
 #pragma unroll
                     for (int h = 0; h < BN / 128; ++h)
@@ -696,16 +688,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mbar_expect_tx(&full[stage], C::TX_BYTES);
                 tma_load_2d(stage_a(stage), &tmA, kb * BK_BYTES, (int)m0, &full[stage]);
-                if (CM > 1) {
-                    // this CTA's 128-row share of B, delivered to the whole cluster
-                    for (int h = (int)rank; h < BN / 128; h += CM)
-                        tma_load_2d_mc(stage_b(stage) + h * 128 * BK_BYTES, &tmB, kb * BK_BYTES, (int)b_row(n0, h),
-                                       &full[stage], (uint16_t)((1u << CM) - 1));
-                } else {
-                    for (int h = 0; h < BN / 128; ++h)
-                        tma_load_2d(stage_b(stage) + h * 128 * BK_BYTES, &tmB, kb * BK_BYTES, (int)b_row(n0, h),
-                                    &full[stage]);
-                }
+                for (int h = 0; h < BN / 128; ++h)
+                    tma_load_2d(stage_b(stage) + h * 128 * BK_BYTES, &tmB, kb * BK_BYTES, (int)b_row(n0, h),
+                                &full[stage]);
                 const uint8_t* sfa = p.a_scales + ((m0 >> 7) * k_atoms + (int64_t)kb * C::SF_CHUNKS) * 512;
                 bulk_load(stage_sfa(stage), sfa, C::SFA_BYTES, &full[stage]);
 #pragma unroll
@@ -780,9 +765,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 if (P2)
-                    tc_commit_mc<2>(&empty[stage], (uint16_t)3);
-                else if (CM > 1)
-                    tc_commit_mc(&empty[stage], (uint16_t)((1u << CM) - 1));
+                    tc_commit_pair(&empty[stage], (uint16_t)3);
                 else
                     tc_commit(&empty[stage]);
                 if (++stage == STAGES) {
@@ -792,7 +775,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) break;
             if (P2)
-                tc_commit_mc<2>(acc_full, (uint16_t)3);
+                tc_commit_pair(acc_full, (uint16_t)3);
             else
                 tc_commit(acc_full);
             acc_phase ^= 1;
@@ -1296,7 +1279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (is_store(EPI) && warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores done with shared memory
     tc_fence_before();
     __syncthreads();
-    if (CM > 1) cluster_sync();  // no peer still multicasts into this CTA
+    if (CM > 1) cluster_sync();  // the peer no longer arrives on this CTA's barriers
     if (warp == 1) {
         tc_fence_after();
         if (P2)
@@ -1324,11 +1307,12 @@ bool get_encode() {
     return g_encode != nullptr;
 }
 
-// K-major FP4 codes [rows][K/2] bytes as a 2D uint8 tensor, box 128 B x 128 rows.
-bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K) {
+// K-major FP4 codes [rows][K/2] bytes as a 2D uint8 tensor, box 128 B x
+// `box_rows` rows (128, or 64 for the B half of a 128-wide pair tile).
+bool make_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t K, int box_rows = 128) {
     cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, 128u};
+    cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, BK_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -1384,7 +1368,8 @@ template <bool NV, int BN, int EPI, int CM, bool P2 = false>
 int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream_t stream) {
     using C = Cfg<NV, BN, EPI, P2>;
     CUtensorMap ta, tb, tc, tsa, tsb;
-    if (!make_map(&ta, g.a_codes, g.M, g.K) || !make_map(&tb, g.b_codes, g.b_rows, g.K)) return FP4_ERR_CUDA;
+    if (!make_map(&ta, g.a_codes, g.M, g.K) || !make_map(&tb, g.b_codes, g.b_rows, g.K, P2 ? BN / 2 : 128))
+        return FP4_ERR_CUDA;
     memset(&tc, 0, sizeof tc);
     memset(&tsa, 0, sizeof tsa);
     memset(&tsb, 0, sizeof tsb);
@@ -1398,14 +1383,16 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
         return FP4_ERR_CUDA;
     auto kern = fp4_gemm_kernel<NV, BN, EPI, CM, P2>;
     int dev = 0;
-    cudaGetDevice(&dev);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP4_ERR_CUDA;
+    static std::mutex mu;
     static bool attr_done[64] = {};
-    if (dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return FP4_ERR_CUDA;
-        if (CM > 1 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
-            return FP4_ERR_CUDA;
-        attr_done[dev] = true;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_done[dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+                return FP4_ERR_CUDA;
+            attr_done[dev] = true;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1497,9 +1484,9 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     }
     if (g.epi == 2) {  // SwiGLU backward: W2 Dgrad, output [M][f]
         const int64_t units_1 = (g.M / BM) * (g.N / 128);
-        if (g.nv) return pair ? launch_t<true, 128, EPI_SWIGLU_BWD, 2>(g, kp, units_1 / 2, stream)
+        if (g.nv) return pair ? launch_t<true, 128, EPI_SWIGLU_BWD, 2, true>(g, kp, units_1 / 2, stream)
                               : launch_t<true, 128, EPI_SWIGLU_BWD, 1>(g, kp, units_1, stream);
-        return pair ? launch_t<false, 128, EPI_SWIGLU_BWD, 2>(g, kp, units_1 / 2, stream)
+        return pair ? launch_t<false, 128, EPI_SWIGLU_BWD, 2, true>(g, kp, units_1 / 2, stream)
                     : launch_t<false, 128, EPI_SWIGLU_BWD, 1>(g, kp, units_1, stream);
     }
     const bool wide = (g.N % 256) == 0;
@@ -1512,17 +1499,16 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
                             : launch_t<false, 128, EPI_STORE_RMS, 1>(g, kp, units_128, stream);
     }
     if (g.nv) {
-        // 256-wide tiles go to the CTA-pair kernel for both formats; with the
-        // scale copies off the MMA thread, NVFP4's twice-as-many copies no
-        // longer make it slower than the multicast kernel (10-12% faster)
+        // an even number of M blocks runs on CTA pairs (M = 256 MMAs), 256 or
+        // 128 columns wide; an odd number on single CTAs
         if (wide) return pair ? launch_t<true, 256, EPI_STORE, 2, true>(g, kp, units_1 / 2, stream)
                               : launch_t<true, 256, EPI_STORE, 1>(g, kp, units_1, stream);
-        return pair ? launch_t<true, 128, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+        return pair ? launch_t<true, 128, EPI_STORE, 2, true>(g, kp, units_1 / 2, stream)
                     : launch_t<true, 128, EPI_STORE, 1>(g, kp, units_1, stream);
     }
     if (wide) return pair ? launch_t<false, 256, EPI_STORE, 2, true>(g, kp, units_1 / 2, stream)
                           : launch_t<false, 256, EPI_STORE, 1>(g, kp, units_1, stream);
-    return pair ? launch_t<false, 128, EPI_STORE, 2>(g, kp, units_1 / 2, stream)
+    return pair ? launch_t<false, 128, EPI_STORE, 2, true>(g, kp, units_1 / 2, stream)
                 : launch_t<false, 128, EPI_STORE, 1>(g, kp, units_1, stream);
 }
 

@@ -22,6 +22,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -691,16 +693,25 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
 // the latency-bound weight and activation producers.)
 unsigned encoder_grid(int64_t n_tiles) { return (unsigned)((n_tiles + 1) / 2); }
 
+// The encoder's shared memory (about 90 KB) is above the 48 KB default, so
+// each instantiation's limit is raised once per device, under a lock.
 template <bool NVR, bool NVC>
 int launch_encoder(const QuantParams& p, cudaStream_t stream) {
     const size_t smem = sizeof(SmemQ);
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return FP4_ERR_CUDA;
-        cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        attr_done = true;
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP4_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_done[dev]) {
+            if (cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess ||
+                cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     100) != cudaSuccess)
+                return FP4_ERR_CUDA;
+            attr_done[dev] = true;
+        }
     }
     const int64_t n_tiles = (p.C / TILE) * (p.R / TILE);
     quantize_tile_kernel<NVR, NVC><<<encoder_grid(n_tiles), THREADS, smem, stream>>>(p);

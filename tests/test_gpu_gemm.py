@@ -154,10 +154,12 @@ def test_route_mismatch_is_rejected():
 
 
 @pytest.mark.parametrize("M,N,K,route", [(384, 384, 512, "mx"), (2048, 4096, 512, "mx"), (2048, 2048, 768, "nv_local"),
-                                         (640, 768, 256, "nv_global")])
+                                         (640, 768, 256, "nv_global"), (1024, 640, 512, "mx"),
+                                         (512, 384, 768, "nv_local"), (256, 128, 256, "nv_global")])
 def test_persistent_tiles_unpaired_and_narrow(M, N, K, route):
     """Shapes that make CTAs loop over several tiles, use unpaired M blocks
-    (no cluster) and the 128-wide N tile; checked on sampled entries."""
+    (single CTAs) and the 128-wide N tile on single CTAs and on CTA pairs
+    (each CTA of a pair loads 64 rows of B); checked on sampled entries."""
     bs, fmt = (32, 0) if route == "mx" else (16, 1)
     a = normal_bf16((M, K), 1.0, M + N, 1)
     b = normal_bf16((N, K), 0.05, M + N, 2)
