@@ -369,9 +369,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1", "data": "synthetic (seeded: X Student-t4 unit var, W N(0,0.02), dY N(0,1e-4))",
-        "config": {"workload": WORKLOAD, "tokens": T, "d_in": D_IN, "d_out": D_OUT, "route": "mxfp4",
-                   "flags": "X col H32, W 2D32, dY row SR + col H32", "out_dtype": "f32",
-                   "l2": "inputs larger than L2 (419 MB bf16 per step)", "parallelism": f"replicas{world}"},
+        "config": main_config(world),
         "tokens_per_s": round(T / (ms * 1e-3) * world, 1),
         "quant_gbs": round(quant_gbs, 1),
         "kernels": kernels,
@@ -541,7 +539,7 @@ def run_legs(args, peaks, only=None) -> dict:
         return out
     # fused SwiGLU FFN, MXFP4, T 16384, d 4096, f 14336
     if only == "stack":
-        return run_stack_leg(args, out)
+        return run_stack_leg(args, out, peaks)
     t4 = config_tensors("c4_swiglu", scale_T=args.tokens)
     X4, W13, W2, DY2 = dev(t4["x"]), dev(t4["w13"]), dev(t4["w2"]), dev(t4["dy2"])
     del t4
@@ -585,7 +583,7 @@ def run_legs(args, peaks, only=None) -> dict:
     torch.cuda.empty_cache()
 
     if not args.no_stack and only is None:
-        run_stack_leg(args, out)
+        run_stack_leg(args, out, peaks)
     return out
 
 
@@ -628,11 +626,40 @@ def run_qkv_rope_leg(T: int = 8192, d: int = 4096, hq: int = 32, hkv: int = 8, S
             "plain_quantize_ms": round(qplain, 4)}
 
 
-def run_stack_leg(args, out: dict) -> dict:
+def stack_producer_bytes(sh, n_blocks: int, local_blocks: int) -> float:
+    """Algorithmic bytes of every producer of one stack step (forward +
+    backward): BF16 inputs read once (twice for NVFP4, whose outer factors
+    need a maximum before the encode), the retained BF16 values written once,
+    and per FP4 view 0.5 B of codes + 1 / block size B of scales per element.
+    The contractions' own operand reads and outputs are not counted: they are
+    inside the FLOP term of the composite roofline."""
+    T, d, f, q = sh.T, sh.d, sh.f, sh.qkv
+    total = 0.0
+    for b in range(n_blocks):
+        nv = b < local_blocks
+        nvx = 2.0 if nv else 0.0                        # the NVFP4 maximum pass
+        v2 = 2 * (0.5 + (1 / 16 if nv else 1 / 32))     # both views
+        W = q * d + d * d + 2 * f * d + d * f
+        total += W * (2 + nvx + v2)                     # 2D weight producers
+        total += 2 * (T * d * (2 + 2 + 2 + nvx + v2) + 4 * T)  # residual-RMSNorm fwd: r, b in; r', views, rstd out
+        total += T * d * (2 + nvx + v2)                 # attention output producer
+        total += T * f * (4 + v2)                       # SwiGLU fwd epilogue: a1, a3 out, views of h
+        total += T * f * 4 + 2 * T * f * v2             # SwiGLU bwd epilogue: a1, a3 in, views of [da1 | da3]
+        total += 2 * T * d * (2 + 2 + 2 + 2 + nvx + v2)  # residual-RMSNorm bwd: dx, r', dres in; dr, views out
+        total += T * q * (2 + nvx + v2)                 # dQKV producer
+    top_nv = n_blocks - 1 < local_blocks
+    total += T * d * (2 + (2.0 if top_nv else 0.0) + 2 * (0.5 + (1 / 16 if top_nv else 1 / 32)))
+    return total
+
+
+def run_stack_leg(args, out: dict, peaks=None) -> dict:
     """The depth-hybrid block stack at T 8192 (blocks 1-27 CTA-local NVFP4,
-    28-32 MXFP4); --stack-blocks keeps the same 27/32 split on fewer blocks."""
+    28-32 MXFP4); --stack-blocks keeps the same 27/32 split on fewer blocks.
+    Ten timed steps; the attention stand-in's gradient copy (not part of the
+    FP4 boundary) is timed by events and taken out of the step time."""
     import torch
     from fp4_quantized_linears_gb300.stack import BlockShape, FP4LinearStack, linear_flops_per_token
+    peaks = peaks or load_peaks()
     nb = args.stack_blocks
     local = (27 * nb) // 32 if nb != 32 else 27
     sh = BlockShape()
@@ -640,11 +667,33 @@ def run_stack_leg(args, out: dict) -> dict:
     g = torch.Generator(device="cuda").manual_seed(5)
     x5 = torch.randn((sh.T, sh.d), generator=g, device="cuda").to(torch.bfloat16)
     dy5 = (torch.randn((sh.T, sh.d), generator=g, device="cuda") * 1e-4).to(torch.bfloat16)
-    ms = _timed(lambda: st.step(x5, dy5, sr_seed=5), 2, 1)
+    steps = args.stack_steps
+    for _ in range(2):
+        st.step(x5, dy5, sr_seed=5)
+    torch.cuda.synchronize()
+    st.time_standin = True
+    st.standin_ms()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        st.step(x5, dy5, sr_seed=5)
+    e1.record()
+    torch.cuda.synchronize()
+    standin = st.standin_ms() / steps
+    ms_all = e0.elapsed_time(e1) / steps
+    ms = ms_all - standin
     fl5 = linear_flops_per_token(sh) * nb * sh.T
+    pb = stack_producer_bytes(sh, nb, local)
+    p_fp4 = peaks["bf16_sus"] * FP4_NOMINAL_OVER_BF16  # a long step: the sustained figure
+    t_roof = fl5 / (p_fp4 * 1e12) + pb / (peaks["hbm"] * 1e9)
     out[f"stack{nb}_hybrid_{local}nv_{nb - local}mx_T8192"] = {
         "ms_per_step": round(ms, 2), "tokens_per_s": round(sh.T / ms * 1e3, 1),
-        "linear_TFLOP/s": round(fl5 / ms / 1e9, 1), "linear_tflop_per_step": round(fl5 / 1e12, 2)}
+        "linear_TFLOP/s": round(fl5 / ms / 1e9, 1), "linear_tflop_per_step": round(fl5 / 1e12, 2),
+        "steps": steps, "standin_copy_ms_excluded": round(standin, 3), "ms_per_step_with_standin": round(ms_all, 2),
+        "producer_GB_per_step": round(pb / 1e9, 2),
+        "roofline": {"composite_ms": round(t_roof * 1e3, 2), "frac": round(t_roof * 1e3 / ms, 4),
+                     "peak_fp4_TFLOP/s": round(p_fp4, 1), "peak_hbm_GB/s": peaks["hbm"],
+                     "peak_note": f"{peaks['src']} bf16 sustained x 6; {peaks['src']} hbm_gbs"}}
     del st, x5, dy5
     torch.cuda.empty_cache()
     return out
@@ -661,72 +710,115 @@ def _cpu_tensors():
     return _CPU_T
 
 
-def cpu_sample_once(tiles: int = 1, seed: int = 1):
-    """One bounded sample of the workload on the CPU oracle: quantize the
-    operand slices that `tiles` 128 x 128 output tiles of each contraction need
-    and contract them.  Returns (flops counted, seconds)."""
-    import oracle
+def cpu_sample_slices(seed: int) -> dict:
+    """The operand slices that one 128 x 128 output tile of each contraction
+    needs (rows of X, W and dY for Fprop / Dgrad, columns of dY and X for
+    Wgrad, full K), chosen by the seed."""
     t = _cpu_tensors()
-    x, w, dy, s = t["x"], t["w"], t["dy"], t["signs"]
+    x, w, dy = t["x"], t["w"], t["dy"]
     rng = np.random.default_rng(seed)
-    flops = 0.0
+    mt = int(rng.integers(0, T // 128)) * 128
+    ot = int(rng.integers(0, D_OUT // 128)) * 128
+    it = int(rng.integers(0, D_IN // 128)) * 128
+    c = np.ascontiguousarray
+    return dict(x_rows=c(x[mt:mt + 128]), w_rows=c(w[ot:ot + 128]), dy_rows=c(dy[mt:mt + 128]),
+                w_cols=c(w[:, it:it + 128]), dy_cols=c(dy[:, ot:ot + 128]), x_cols=c(x[:, it:it + 128]),
+                signs=t["signs"])
+
+
+def cpu_sample_task(sl: dict):
+    """One bounded sample on the CPU oracle, as it stands: quantize the
+    slices and contract them.  Returns (FLOPs counted, seconds)."""
+    import oracle
     t0 = time.perf_counter()
-    for _ in range(tiles):
-        mt = int(rng.integers(0, T // 128)) * 128
-        ot = int(rng.integers(0, D_OUT // 128)) * 128
-        it = int(rng.integers(0, D_IN // 128)) * 128
-        # Fprop tile: rows mt of X, rows ot of W
-        a = oracle.quantize(np.ascontiguousarray(x[mt:mt + 128]), "mx", "row")
-        b = oracle.quantize(np.ascontiguousarray(w[ot:ot + 128]), "mx", "row", weight2d=True)
-        oracle.gemm(a, b)
-        # Dgrad tile: rows mt of dY (SR), columns it of W
-        a = oracle.quantize(np.ascontiguousarray(dy[mt:mt + 128]), "mx", "row", sr=True, seed=1)
-        b = oracle.quantize(np.ascontiguousarray(w[:, it:it + 128]), "mx", "col", weight2d=True)
-        oracle.gemm(a, b)
-        # Wgrad tile: columns ot of dY, columns it of X (both H32)
-        a = oracle.quantize(np.ascontiguousarray(dy[:, ot:ot + 128]), "mx", "col", hadamard=True, signs=s)
-        b = oracle.quantize(np.ascontiguousarray(x[:, it:it + 128]), "mx", "col", hadamard=True, signs=s)
-        oracle.gemm(a, b)
-        flops += 2.0 * 128 * 128 * (D_IN + D_OUT + T)
-    return flops, time.perf_counter() - t0
+    a = oracle.quantize(sl["x_rows"], "mx", "row")
+    b = oracle.quantize(sl["w_rows"], "mx", "row", weight2d=True)
+    oracle.gemm(a, b)
+    a = oracle.quantize(sl["dy_rows"], "mx", "row", sr=True, seed=1)
+    b = oracle.quantize(sl["w_cols"], "mx", "col", weight2d=True)
+    oracle.gemm(a, b)
+    a = oracle.quantize(sl["dy_cols"], "mx", "col", hadamard=True, signs=sl["signs"])
+    b = oracle.quantize(sl["x_cols"], "mx", "col", hadamard=True, signs=sl["signs"])
+    oracle.gemm(a, b)
+    return 2.0 * 128 * 128 * (D_IN + D_OUT + T), time.perf_counter() - t0
+
+
+class CpuPool:
+    """The oracle on every host core: one spawned worker process per core
+    (spawned, so no worker inherits a CUDA context), each running one sample
+    at a time."""
+
+    def __init__(self, cores: int | None = None):
+        import multiprocessing as mp
+        import oracle
+        oracle.build()
+        self.cores = max(1, cores or os.cpu_count() or 1)
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+
+    def round(self, seed0: int):
+        """One sample per core; returns (FLOPs, wall seconds)."""
+        tasks = [cpu_sample_slices(seed0 + i) for i in range(self.cores)]
+        t0 = time.perf_counter()
+        res = self.pool.map(cpu_sample_task, tasks)
+        return sum(r[0] for r in res), time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+CPU_SAMPLE = ("one 128x128 output tile of each of Fprop, Dgrad, Wgrad at the full K, with the quantization "
+              "of the operand slices it needs, per core, on the C oracle")
 
 
 def cpu_baseline_sample(seconds_target: float = 10.0) -> dict:
-    flops, secs = 0.0, 0.0
-    n = 0
-    while secs < seconds_target or n == 0:
-        f, s = cpu_sample_once(1, seed=100 + n)
-        flops += f
-        secs += s
-        n += 1
-    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} x (one 128x128 output tile of each of Fprop, Dgrad, Wgrad at the full K, with the "
-                      f"quantization of the operand slices it needs), single-threaded C oracle, {secs:.1f} s"}
+    pool = CpuPool()
+    try:
+        pool.round(0)  # workers start and load the oracle
+        flops, secs, n = 0.0, 0.0, 0
+        while secs < seconds_target or n == 0:
+            f, s_ = pool.round(100 + n * pool.cores)
+            flops += f
+            secs += s_
+            n += 1
+    finally:
+        pool.close()
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{n} rounds x {pool.cores} cores x ({CPU_SAMPLE}), {secs:.1f} s wall"}
+
+
+def main_config(world: int) -> dict:
+    return {"workload": WORKLOAD, "tokens": T, "d_in": D_IN, "d_out": D_OUT, "route": "mxfp4",
+            "flags": "X col H32, W 2D32, dY row SR + col H32", "out_dtype": "f32",
+            "l2": "inputs larger than L2 (419 MB bf16 per step)", "parallelism": f"replicas{world}"}
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on every host core;
+    each step is one bounded sample per core of the same workload."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import oracle
-    oracle.build()
-    for i in range(args.warmup):
-        cpu_sample_once(1, seed=i)
-    flops, secs = 0.0, 0.0
-    for i in range(args.steps):
-        f, s = cpu_sample_once(1, seed=1000 + i)
-        flops += f
-        secs += s
+    pool = CpuPool()
+    try:
+        for i in range(args.warmup):
+            pool.round(i * pool.cores)
+        flops, secs = 0.0, 0.0
+        for i in range(args.steps):
+            f, s_ = pool.round(1000 + i * pool.cores)
+            flops += f
+            secs += s_
+    finally:
+        pool.close()
     v = flops / secs / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same seeded tensors as the GPU arm)",
-        "config": {"workload": WORKLOAD, "tokens": T, "d_in": D_IN, "d_out": D_OUT, "route": "mxfp4"},
-        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                         "sample": "per step: one 128x128 output tile of each of Fprop, Dgrad, Wgrad at the full K "
-                                   "plus the quantization of the operand slices it needs (single-threaded C oracle)"},
+        "config": main_config(1),
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": pool.cores, "kind": "oracle",
+                         "sample": f"per step: {CPU_SAMPLE}"},
         "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -743,6 +835,7 @@ def main():
     ap.add_argument("--no-legs", action="store_true", help="only the main workload")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-block stack leg")
     ap.add_argument("--stack-blocks", type=int, default=32, help="blocks of the stack leg (profiling-sized runs)")
+    ap.add_argument("--stack-steps", type=int, default=10, help="timed steps of the stack leg")
     ap.add_argument("--only", choices=["nvfp4", "swiglu", "stack", "diagnostic", "qkv"], default=None,
                     help="run just one of the other legs (sized by --tokens) and print its numbers")
     ap.add_argument("--tokens", type=int, default=None,

@@ -49,7 +49,8 @@ FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
 // ----------------------------------------------------- packed binary32 ----
 // Two binary32 lanes per instruction (f32x2 arithmetic of sm_100 and later):
 // each lane is the correctly rounded result of the scalar operation on
-// that lane (to nearest even, or upward for add_rp), so a pair op and two scalar ops give the same bits.
+// that lane (to nearest even, or upward for fma_rp), so a pair op and two
+// scalar ops give the same bits.
 FP4_DEV void f32x2_add(float& x, float& y, float a0, float a1, float b0, float b1) {
     asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
         "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
@@ -60,14 +61,14 @@ FP4_DEV void f32x2_sub(float& x, float& y, float a0, float a1, float b0, float b
         "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
         : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
-FP4_DEV void f32x2_add_rp(float& x, float& y, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "add.rp.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
 FP4_DEV void f32x2_fma(float& x, float& y, float a0, float a1, float b0, float b1, float c0, float c1) {
     asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
         "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+FP4_DEV void f32x2_fma_rp(float& x, float& y, float a0, float a1, float b0, float b1, float c0, float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rp.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
         : "=f"(x), "=f"(y) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 FP4_DEV void f32x2_mul(float& x, float& y, float a0, float a1, float b0, float b1) {
@@ -86,30 +87,42 @@ FP4_DEV float max3_abs_nan(float m, float a, float b) {
 // --------------------------------------------------------------- E2M1 SR ---
 // Adjacent-bin stochastic rounding (Sec. 2.5, Eq. 9): with q- <= |v| < q+
 // neighbouring grid values, round up iff u * 2^-16 < p = (|v| - q-) / (q+ - q-)
-// for a 16-bit uniform u; |v| >= 6 saturates.  Evaluated exactly, two values
-// at a time (u_x = rw & 0xFFFF for x, u_y = rw >> 16 for y):
-//   |v| in [1, 6): the grid has one fraction bit, q- is |v| truncated to it
-//     (code (bits >> 22) - 252) and p = low22 / 2^22 (the 22 fraction bits
-//     below it).  Adding 2^22 - 1 - u * 2^6 to the bits carries into the grid
-//     bit exactly when u * 2^6 < low22, i.e. when the value rounds up;
-//   |v| < 1: the grid 0, 0.5, 1 has step 0.5, so the code is
-//     ceil(2|v| - u * 2^-16) = ceil((|v| * 2^17 - u) / 2^16).  The FMA
-//     |v| * 2^17 - u is exact where it can reach 2^16 (|v| >= 0.5) and keeps
-//     its sign elsewhere; a round-upward add of 1.5 * 2^39 (float spacing 2^16
-//     there) takes the ceiling and leaves the code in the low bits.
+// for a 16-bit uniform u; |v| >= 6 saturates.  Evaluated exactly on the bits:
+//   |v| >= 1: the grid has one fraction bit, q- is |v| truncated to it (code
+//     (bits - 0x3F000000) >> 22) and p = low22 / 2^22 (the 22 fraction bits
+//     below it).  Adding r = 2^22 - 1 - u * 2^6 to the bits carries into the
+//     grid bit exactly when u * 2^6 < low22, i.e. when the value rounds up;
+//   |v| < 1: the grid 0, 0.5, 1 has step 0.5 = the grid step of [1, 2), so
+//     |v| is first mapped to b = (|v| + 1) / 2 in [0.5, 1], rounded upward to
+//     binary32; b has the same fraction of a grid step (rounded up to a
+//     multiple of 2^-22 of the step, which leaves the comparison with u * 2^-16
+//     unchanged), and the same carry rule gives codes 0, 1, 2.  Because
+//     (|v| + 1) / 2 > |v| exactly when |v| < 1, b = max(|v|, that) selects the
+//     right form without a branch (integer max on the bit patterns).
+// sr_code_pair takes the two scaled magnitudes and returns their two 3-bit
+// magnitude codes (x in the low nibble); rw holds u_x in its low and u_y in
+// its high 16 bits.
+FP4_DEV uint32_t sr_code_pair(float ax, float ay, uint32_t rw) {
+    float cx, cy;
+    f32x2_fma_rp(cx, cy, ax, ay, 0.5f, 0.5f, 0.5f, 0.5f);  // fl_up((|v| + 1) / 2)
+    const uint32_t tx = max(__float_as_uint(ax), __float_as_uint(cx));
+    const uint32_t ty = max(__float_as_uint(ay), __float_as_uint(cy));
+    const uint32_t hx = min((tx + (((rw << 6) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
+    const uint32_t hy = min((ty + (((rw >> 10) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
+    return hx | (hy << 4);
+}
 FP4_DEV uint32_t e2m1x2_sr(float x, float y, uint32_t rw) {
     const uint32_t bx = __float_as_uint(x), by = __float_as_uint(y);
-    const uint32_t ax = bx & 0x7FFFFFFFu, ay = by & 0x7FFFFFFFu;
-    const uint32_t hx = min((ax + (((rw << 6) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
-    const uint32_t hy = min((ay + (((rw >> 10) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
-    float nx, ny, zx, zy;
-    f32x2_sub(nx, ny, 8388608.0f, 8388608.0f, __uint_as_float(__byte_perm(rw, 0x4B000000u, 0x7610)),
-              __uint_as_float(__byte_perm(rw, 0x4B000000u, 0x7632)));  // -u_x, -u_y (exact)
-    f32x2_fma(zx, zy, __uint_as_float(ax), __uint_as_float(ay), 131072.0f, 131072.0f, nx, ny);
-    f32x2_add_rp(zx, zy, zx, zy, 824633720832.0f, 824633720832.0f);  // 1.5 * 2^39 = 0x53400000
-    const uint32_t cx = ax >= 0x3F800000u ? hx : __float_as_uint(zx) - 0x53400000u;
-    const uint32_t cy = ay >= 0x3F800000u ? hy : __float_as_uint(zy) - 0x53400000u;
-    return (cx | ((bx >> 28) & 8u)) | ((cy | ((by >> 28) & 8u)) << 4);
+    return sr_code_pair(fabsf(x), fabsf(y), rw) | ((bx >> 28) & 8u) | ((by >> 24) & 0x80u);
+}
+// The two bf16 values of one word (low half first) scaled by a non-negative
+// multiplier (fl32(x * mult), as the RN path) and rounded stochastically; the
+// codes keep the inputs' sign bits.
+FP4_DEV uint32_t e2m1x2_sr_bf16(uint32_t w, float mult, uint32_t rw) {
+    const uint32_t wa = w & 0x7FFF7FFFu;
+    float ax, ay;
+    f32x2_mul(ax, ay, __uint_as_float(wa << 16), __uint_as_float(wa & 0xFFFF0000u), mult, mult);
+    return sr_code_pair(ax, ay, rw) | ((w >> 12) & 8u) | ((w >> 24) & 0x80u);
 }
 
 // --------------------------------------------------------------- E4M3 ------

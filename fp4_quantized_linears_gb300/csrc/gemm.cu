@@ -69,10 +69,8 @@ constexpr int BK = 256;  // FP4 elements per stage: 128-byte rows, 128-byte swiz
 constexpr int BK_BYTES = BK / 2;
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
 constexpr int MAX_STAGES = 8;
-constexpr int EPI_WARPS = 8;
-constexpr int SF_WARP = 2 + EPI_WARPS;  // the first of the warps that move scale factors into TMEM
-constexpr int SF_WARPS = 2;             // each copies every SF_WARPS-th scale chunk of a stage
-constexpr int THREADS = 32 * (SF_WARP + SF_WARPS);
+constexpr int EPI_WARPS = 8;  // epilogue warps (16 for the SwiGLU backward; warps 2 .. 2 + count - 1)
+constexpr int SF_WARPS = 2;   // after the epilogue warps: each copies every SF_WARPS-th scale chunk of a stage
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;  // first TMEM column of the scale-factor region
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
@@ -300,6 +298,20 @@ FP4_DEV void tmem_ld64(uint32_t taddr, uint32_t* r) {
         : "r"(taddr)
         : "memory");
 }
+FP4_DEV void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31"
+        "}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
 // Two 64-column loads (at ta and tb) under one wait.
 FP4_DEV void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t* a, uint32_t* b) {
     asm volatile(
@@ -404,31 +416,56 @@ FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
     return (uint32_t)(e + 127);
 }
 
-// MX block of 32 values with stochastic rounding (logical indices 8*g0 ..).
-FP4_DEV uint32_t mx_block_sr(const float* v, uint64_t g0, uint64_t seed, uint64_t offset, uint4& packed) {
-    float amf = 0.0f;
+// fp32 bit pattern of the larger magnitude in a word of two bf16 maxima
+FP4_DEV uint32_t lanes_max_f32bits(uint32_t m2) { return max(m2 << 16, m2 & 0xFFFF0000u); }
+
+// MX block of the 32 bf16 values of 16 words (logical indices 8*g0 ..), with
+// stochastic rounding: scale byte and 16 bytes of codes.  The block maximum
+// is taken on the bf16 magnitudes (their unsigned order is the numeric one;
+// a NaN still ends at or above the infinity pattern).
+FP4_DEV uint32_t mx_words_sr(const uint32_t* w, uint64_t g0, uint64_t seed, uint64_t offset, uint4& packed) {
+    uint32_t m2 = 0;
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) amf = max3_abs_nan(amf, v[i], v[i + 1]);
-    const uint32_t am = __float_as_uint(amf);
+    for (int i = 0; i < 16; i += 2) m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
+    const uint32_t am = lanes_max_f32bits(m2);
     if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
     const int e = e8m0_exponent_up(am);
     const float mult = exp2_neg(e);
-    uint32_t w[4];
+    uint32_t out[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint4 rb = sr_bits8(g0 + q, seed, offset);
-        uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
+        const uint4 rb = sr_bits8(g0 + q, seed, offset);
+        const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16(w[4 * q + b], mult, rw[b]) << (8 * b);
+        out[q] = word;
+    }
+    packed = make_uint4(out[0], out[1], out[2], out[3]);
+    return (uint32_t)(e + 127);
+}
+
+// MX block of the low (h = 0) or high (h = 1) bf16 lanes of 32 words, round
+// to nearest; am = fp32 bits of the block's maximum magnitude.
+FP4_DEV uint32_t mx_lane_rn(const uint32_t* w, int h, uint32_t am, uint4& packed) {
+    if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
+    const int e = e8m0_exponent_up(am);
+    const float mult = exp2_neg(e);
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
         uint32_t word = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            int i = q * 8 + b * 2;
+            const int i = q * 8 + b * 2;
             float x, y;
-            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
-            word |= e2m1x2_sr(x, y, rw[b]) << (8 * b);
+            f32x2_mul(x, y, h ? bf16_hi(w[i]) : bf16_lo(w[i]), h ? bf16_hi(w[i + 1]) : bf16_lo(w[i + 1]), mult,
+                      mult);
+            word |= e2m1x2_rn(x, y) << (8 * b);
         }
-        w[q] = word;
+        out[q] = word;
     }
-    packed = make_uint4(w[0], w[1], w[2], w[3]);
+    packed = make_uint4(out[0], out[1], out[2], out[3]);
     return (uint32_t)(e + 127);
 }
 
@@ -461,6 +498,12 @@ FP4_DEV void store_bf16x32(uint16_t* dst, const float* v) {
 // store's register allocation is untouched)
 enum { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_QKV_ROPE = 3, EPI_STORE_RMS = 4 };
 __host__ __device__ constexpr bool is_store(int epi) { return epi == EPI_STORE || epi == EPI_STORE_RMS; }
+// The SwiGLU backward's epilogue (SiLU derivative, two SR row views, two
+// transposed column views per tile) is latency-bound: it runs on 16 warps,
+// each thread holding one row x 32 columns; the others on 8 (one row x 64 or
+// 128 columns).
+__host__ __device__ constexpr int epi_warps(int epi) { return epi == EPI_SWIGLU_BWD ? 16 : EPI_WARPS; }
+__host__ __device__ constexpr int kthreads(int epi) { return 32 * (2 + epi_warps(epi) + SF_WARPS); }
 
 struct KParams {
     const uint8_t* a_scales;
@@ -544,7 +587,7 @@ struct Cfg {
 };
 
 template <bool NV, int BN, int EPI, int CM, bool P2 = false>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(kthreads(EPI), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
                     const __grid_constant__ CUtensorMap tmSB, KParams p) {
@@ -554,6 +597,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int G = P2 ? 2 : 1;       // tcgen05 CTA group
     constexpr int MMA_M = P2 ? 2 * BM : BM;
     constexpr int STAGES = C::STAGES;
+    constexpr int EW = epi_warps(EPI);  // epilogue warps
+    constexpr int SF_WARP = 2 + EW;     // the first of the warps that move scale factors into TMEM
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // The ring's 128-byte-swizzled stages need 1 KiB alignment, and the
     // budget leaves no slack to realign: a kernel whose dynamic shared base
@@ -612,9 +657,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         mbar_init(sf_drain, SF_WARPS);
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, P2 ? 2 * EPI_WARPS : EPI_WARPS);  // pair: both CTAs' epilogues, on the leader
+        mbar_init(acc_empty, P2 ? 2 * EW : EW);  // pair: both CTAs' epilogues, on the leader
         mbar_init(drain_bar, 1);
-        mbar_init(epi_bar, EPI_WARPS * 32);
+        mbar_init(epi_bar, EW);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -832,12 +877,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         // every copy issued has completed before TMEM can be released
         tc_commit<G>(sf_drain);
         mbar_wait(sf_drain, 0);
-    } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
+    } else if (warp >= 2 && warp < 2 + EW) {
         // ------------------------------------------------ epilogue --------
         const int q = warp & 3;               // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;     // column half
+        const int half = (warp - 2) >> 2;     // column half (SwiGLU backward: column quarter)
         const int lr = q * 32 + lane;         // row within the tile
-        const int et = (warp - 2) * 32 + lane;  // epilogue thread index 0..255
+        const int et = (warp - 2) * 32 + lane;  // epilogue thread index 0 .. 32 * EW - 1
         uint32_t acc_phase = 0, epi_phase = 0;
         bool epi_ok = true;
         // the accumulator is free once every epilogue warp has read it; in
@@ -851,9 +896,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive(acc_empty);
             }
         };
-        // bounded barrier among the 256 epilogue threads
+        // bounded barrier among the epilogue warps: one arrive per warp after
+        // the warp's own lanes have synchronised
         auto epi_sync = [&]() {
-            mbar_arrive(epi_bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_bar);
             if (!mbar_wait(epi_bar, epi_phase)) {
                 *abort_flag = 1;
                 epi_ok = false;
@@ -864,12 +911,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             int64_t m0, n0;
             unit_coords(u, m0, n0);
             if constexpr (EPI == EPI_SWIGLU_BWD) {
-                // this thread's retained a1 / a3 (one 128-byte row segment
+                // this thread's retained a1 / a3 (one 64-byte row segment
                 // each) do not depend on the accumulator: start moving them
                 // into L2 while the tile's MMAs run
-                const int64_t off = (m0 + lr) * p.f + n0 + 64 * half;
-                bulk_prefetch_l2(p.a1 + off, 128);
-                bulk_prefetch_l2(p.a3 + off, 128);
+                const int64_t off = (m0 + lr) * p.f + n0 + 32 * half;
+                bulk_prefetch_l2(p.a1 + off, 64);
+                bulk_prefetch_l2(p.a3 + off, 64);
             }
             if (!mbar_wait(acc_full, acc_phase)) {
                 *abort_flag = 1;
@@ -1158,11 +1205,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     epi_sync();
                 }
             } else {
-                // EPI_SWIGLU_BWD: dh for output columns [64*half, 64*half + 64)
-                uint32_t dp[32];  // bf16x2 of dh (64 columns)
+                // EPI_SWIGLU_BWD: dh for output columns [oc, oc + 32) of this
+                // thread's row
+                const int oc = 32 * half;
+                const int64_t n = n0 + oc;
+                uint32_t dp[16];  // bf16x2 of dh
                 {
-                    uint32_t r[64];
-                    tmem_ld64(lane_base + 64 * half, r);
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + oc, r);
                     tc_fence_before();
                     release_acc();
                     float alpha = 1.0f;
@@ -1170,30 +1220,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                         alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
                                           __fdiv_rn(1.0f, p.b_outer[p.b_outer_count == 1 ? 0 : (n0 >> 7)]));
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < 16; ++i)
                         dp[i] = bf16x2_rn(__uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
                 }
                 uint16_t* s1 = reinterpret_cast<uint16_t*>(staging);
                 uint16_t* s3 = s1 + BM * ST_LDS;
                 uint8_t* atoms = staging + 2 * BM * ST_LDS * 2;  // row da1, row da3, col da1, col da3
                 const int64_t f2 = 2 * p.f;
+                if (p.tap0) store_words16(p.tap0 + m * p.f + n, dp);
+                // da1 = bf16(dh * a3 * SiLU'(a1)), da3 = bf16(dh * SiLU(a1)), as bf16x2 words
+                uint32_t q1[16], q3[16];
+                {
+                    const uint4* pa1 = reinterpret_cast<const uint4*>(p.a1 + m * p.f + n);
+                    const uint4* pa3 = reinterpret_cast<const uint4*>(p.a3 + m * p.f + n);
+                    uint4 v1[4], v3[4];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int oc = 64 * half + 32 * c;
-                    const int64_t n = n0 + oc;
-                    if (p.tap0) store_words16(p.tap0 + m * p.f + n, dp + 16 * c);
-                    float d1[32], d3[32];
-                    uint32_t q1[16], q3[16];
-                    const uint16_t* pa1 = p.a1 + m * p.f + n;
-                    const uint16_t* pa3 = p.a3 + m * p.f + n;
+                    for (int i = 0; i < 4; ++i) {
+                        v1[i] = pa1[i];
+                        v3[i] = pa3[i];
+                    }
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        const uint4 v1 = *reinterpret_cast<const uint4*>(pa1 + i);
-                        const uint4 v3 = *reinterpret_cast<const uint4*>(pa3 + i);
-                        const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t w1[4] = {v1[i].x, v1[i].y, v1[i].z, v1[i].w};
+                        const uint32_t w3[4] = {v3[i].x, v3[i].y, v3[i].z, v3[i].w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint32_t wg = dp[16 * c + i / 2 + j];
+                            const uint32_t wg = dp[4 * i + j];
                             float o1[2], o3[2];
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
@@ -1205,57 +1257,50 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 o1[e] = g * y * dsilu;
                                 o3[e] = g * (x * sg);
                             }
-                            q1[i / 2 + j] = bf16x2_rn(o1[0], o1[1]);
-                            q3[i / 2 + j] = bf16x2_rn(o3[0], o3[1]);
+                            q1[4 * i + j] = bf16x2_rn(o1[0], o1[1]);
+                            q3[4 * i + j] = bf16x2_rn(o3[0], o3[1]);
                         }
                     }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        d1[2 * i] = bf16_lo(q1[i]);
-                        d1[2 * i + 1] = bf16_hi(q1[i]);
-                        d3[2 * i] = bf16_lo(q3[i]);
-                        d3[2 * i + 1] = bf16_hi(q3[i]);
-                    }
-                    if (p.tap1) {
-                        store_words16(p.tap1 + m * f2 + n, q1);
-                        store_words16(p.tap1 + m * f2 + p.f + n, q3);
-                    }
-                    if (p.quantize) {
-                        uint4 pk;
-                        uint32_t sc = mx_block_sr(d1, (uint64_t)(m * f2 + n) >> 3, p.seed, p.offset, pk);
-                        *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + (n >> 1)) = pk;
-                        atoms[atom_off(lr, oc >> 5)] = (uint8_t)sc;
-                        sc = mx_block_sr(d3, (uint64_t)(m * f2 + p.f + n) >> 3, p.seed, p.offset, pk);
-                        *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + ((p.f + n) >> 1)) = pk;
-                        atoms[512 + atom_off(lr, oc >> 5)] = (uint8_t)sc;
-                        store_words16(s1 + lr * ST_LDS + oc, q1);
-                        store_words16(s3 + lr * ST_LDS + oc, q3);
-                    }
+                }
+                if (p.tap1) {
+                    store_words16(p.tap1 + m * f2 + n, q1);
+                    store_words16(p.tap1 + m * f2 + p.f + n, q3);
                 }
                 if (p.quantize) {
+                    // row views of [da1 | da3] (stochastic rounding), one block each
+                    uint4 pk;
+                    uint32_t sc = mx_words_sr(q1, (uint64_t)(m * f2 + n) >> 3, p.seed, p.offset, pk);
+                    *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + (n >> 1)) = pk;
+                    atoms[atom_off(lr, half)] = (uint8_t)sc;
+                    sc = mx_words_sr(q3, (uint64_t)(m * f2 + p.f + n) >> 3, p.seed, p.offset, pk);
+                    *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + ((p.f + n) >> 1)) = pk;
+                    atoms[512 + atom_off(lr, half)] = (uint8_t)sc;
+                    store_words16(s1 + lr * ST_LDS + oc, q1);
+                    store_words16(s3 + lr * ST_LDS + oc, q3);
                     epi_sync();
                     if (!epi_ok) break;
-                    // column pairs: each thread reads 32 bf16x2 words down a pair of
-                    // columns (one 32-bit load per two values) and encodes both
-#pragma unroll 1
-                    for (int k = 0; k < 2; ++k) {
-                        const int idx = et + 256 * k, which = idx >> 8, j = (idx >> 6) & 3, cp = idx & 63;
+                    // column views: thread = (da1 or da3, 32-row block j, column
+                    // pair cp); it reads 32 bf16x2 words down the pair (one 32-bit
+                    // load per two values) and encodes both columns
+                    {
+                        const int which = et >> 8, j = (et >> 6) & 3, cp = et & 63;
                         const uint16_t* src = which ? s3 : s1;
                         uint32_t w[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             w[i] = *reinterpret_cast<const uint32_t*>(&src[(32 * j + i) * ST_LDS + 2 * cp]);
+                        uint32_t m2 = 0;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int cidx = 2 * cp + h;
-                            float v[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
-                            uint4 pk;
-                            uint32_t sc = mx_block_rn(v, pk);
+                            uint4 pkc;
+                            const uint32_t scc = mx_lane_rn(w, h, h ? (m2 & 0xFFFF0000u) : (m2 << 16), pkc);
                             const int64_t srow = (which ? p.f : 0) + n0 + cidx;
-                            *reinterpret_cast<uint4*>(p.q_col_codes + srow * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pk;
-                            atoms[1024 + which * 512 + atom_off(cidx, j)] = (uint8_t)sc;
+                            *reinterpret_cast<uint4*>(p.q_col_codes + srow * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pkc;
+                            atoms[1024 + which * 512 + atom_off(cidx, j)] = (uint8_t)scc;
                         }
                     }
                     epi_sync();
@@ -1396,7 +1441,7 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(kthreads(EPI));
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
     int max_clusters = sm_count() / CM;

@@ -103,25 +103,21 @@ FP4_DEV uint4 pack_rn32(const float* v, float m0, float m1) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Stochastic rounding of 32 values (logical indices 8*g0 .. 8*g0+31).
-FP4_DEV uint4 pack_sr32(const float* v, float m0, float m1, uint64_t g0, uint64_t seed, uint64_t offset) {
-    uint32_t w[4];
+// Stochastic rounding of the 32 bf16 values of 16 words (logical indices
+// 8*g0 .. 8*g0+31), scaled by m0 (values 0..15) and m1 (16..31).
+FP4_DEV uint4 pack_sr32(const uint32_t* w, float m0, float m1, uint64_t g0, uint64_t seed, uint64_t offset) {
+    uint32_t out[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint4 rb = sr_bits8(g0 + q, seed, offset);
-        uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
-        float mult = q < 2 ? m0 : m1;
+        const uint4 rb = sr_bits8(g0 + q, seed, offset);
+        const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
+        const float mult = q < 2 ? m0 : m1;
         uint32_t word = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            int i = q * 8 + b * 2;
-            float x, y;
-            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
-            word |= e2m1x2_sr(x, y, rw[b]) << (8 * b);
-        }
-        w[q] = word;
+        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16(w[4 * q + b], mult, rw[b]) << (8 * b);
+        out[q] = word;
     }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // Butterfly stages of strides 1 .. H/2 on each H-value group of 32
@@ -443,17 +439,17 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 segment_scale<true>(max(lane_lo_f32bits(a0), lane_hi_f32bits(a0)),
                                     max(lane_lo_f32bits(a1), lane_hi_f32bits(a1)), senc_row, s.row_sc, r, j, m0, m1);
             }
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                v[2 * i] = bf16_lo(w[i]);
-                v[2 * i + 1] = bf16_hi(w[i]);
-            }
             uint4 packed;
             if (sr) {
                 const uint64_t g0 = (uint64_t)(((r0 + r) * p.C + c0 + 32 * j) >> 3);
-                packed = pack_sr32(v, m0, m1, g0, p.seed, p.offset);
+                packed = pack_sr32(w, m0, m1, g0, p.seed, p.offset);
             } else {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    v[2 * i] = bf16_lo(w[i]);
+                    v[2 * i + 1] = bf16_hi(w[i]);
+                }
                 packed = pack_rn32(v, m0, m1);
             }
             *reinterpret_cast<uint4*>(&s.row_codes[r * 64 + j * 16]) = packed;

@@ -54,6 +54,17 @@ class _Block:
     s: dict = field(default_factory=dict)   # saved forward state
 
 
+def sr_offset(step: int, block: int, k: int) -> int:
+    """Philox counter offset of stochastically rounded producer k of block
+    `block` in training step `step`.  Seeds and counter offsets are state
+    that must never repeat across steps (Sec. 2.5; Appendix A.1 keeps them in
+    the checkpoint), so the step index fills the upper 32 bits and
+    (block, producer) the lower ones: no two producers of a run share draws."""
+    if not (0 <= step < (1 << 32) and 0 <= block < (1 << 27) and 0 <= k < 16):
+        raise ValueError("SR offset out of range")
+    return (step << 32) | (16 * block + k)
+
+
 def linear_flops_per_token(sh: BlockShape) -> float:
     """Fprop + Dgrad + Wgrad FLOPs of one block's linears per token."""
     per = sh.d * sh.qkv + sh.d * sh.d + 2 * sh.d * sh.f + sh.f * sh.d
@@ -79,6 +90,9 @@ class FP4LinearStack:
             self.blocks.append(_Block(route, w))
         self.g1 = torch.ones(d, dtype=torch.bfloat16, device=self.dev)
         self.g2 = torch.ones(d, dtype=torch.bfloat16, device=self.dev)
+        self.step_index = 0          # training steps taken: part of every SR counter offset
+        self.time_standin = False    # record CUDA events around the attention stand-in's copy
+        self._standin_events = []
         self._alloc()
 
     # ------------------------------------------------------------ buffers --
@@ -157,25 +171,27 @@ class FP4LinearStack:
             h_prev, f_prev = s["r2"], s["f"]
         return h_prev, f_prev
 
-    def backward(self, dy: torch.Tensor, sr_seed: int = 1):
+    def backward(self, dy: torch.Tensor, sr_seed: int = 1, step: int | None = None):
         d, f = self.sh.d, self.sh.f
+        st = self.step_index if step is None else step
+        nb = len(self.blocks)
         top = self.blocks[-1]
         dF = self.gviews[top.route]["dF"]
-        fp4_quantize(dy, top.route, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=0, row_out=dF[0], col_out=dF[1],
-                     workspace=self.ws)
+        fp4_quantize(dy, top.route, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=sr_offset(st, nb, 0), row_out=dF[0],
+                     col_out=dF[1], workspace=self.ws)
         dh_out = dy
-        for i in range(len(self.blocks) - 1, -1, -1):
+        for i in range(nb - 1, -1, -1):
             blk = self.blocks[i]
             r, s, wv, dw, gv = blk.route, blk.s, blk.wv, blk.dw, self.gviews[blk.route]
-            off = 16 * i
+            off1, off2, off3, off4 = (sr_offset(st, i, k) for k in (1, 2, 3, 4))
             # FFN: W2 Wgrad, fused W2 Dgrad + SiLU derivative, W1/W3 Dgrad and Wgrad
             fp4_linear_wgrad(dF[1], s["h"][1], dw["w2"])
             if r == "mx":
-                fp4_swiglu_bwd(dF[0], wv["w2"][1], f, s["a1"], s["a3"], sr_seed, off + 1, da13_row=gv["da13"][0],
+                fp4_swiglu_bwd(dF[0], wv["w2"][1], f, s["a1"], s["a3"], sr_seed, off1, da13_row=gv["da13"][0],
                                da13_col=gv["da13"][1])
             else:
                 fp4_swiglu_bwd(dF[0], wv["w2"][1], f, s["a1"], s["a3"], da13_tap=self.da13, quantize=False)
-                fp4_quantize(self.da13, r, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=off + 1,
+                fp4_quantize(self.da13, r, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=off1,
                              row_out=gv["da13"][0], col_out=gv["da13"][1], workspace=self.ws)
             fp4_linear_dgrad_rmsnorm(gv["da13"][0], wv["w13"][1], s["r2"], s["rstd2"], self.g2, dx=self.dy,
                                      part=self.part)
@@ -183,13 +199,21 @@ class FP4LinearStack:
             # residual-RMSNorm backward -> gradient of r2 and its views (the O projection's dY)
             dr2 = self.dr2
             fp4_residual_rmsnorm_bwd_parts(self.dy, self.part, s["r2"], s["rstd2"], self.g2, dh_out, r, 3, True,
-                                           sr_seed, off + 2, dr=dr2, dr_row=gv["dr2"][0], dr_col=gv["dr2"][1],
+                                           sr_seed, off2, dr=dr2, dr_row=gv["dr2"][0], dr_col=gv["dr2"][1],
                                            workspace=self.ws)
             fp4_linear_wgrad(gv["dr2"][1], s["attn"][1], dw["o"])
             fp4_linear_dgrad(gv["dr2"][0], wv["o"][1], self.dattn, FP4_OUT_BF16)
-            # attention stand-in backward: dQKV = [dattn | 0 | 0]
+            # attention stand-in backward: dQKV = [dattn | 0 | 0] (a copy that
+            # stands in for the attention core, which is not part of the FP4
+            # boundary; its time can be recorded and taken out)
+            if self.time_standin:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record()
             self.dqkv[:, :d].copy_(self.dattn)
-            fp4_quantize(self.dqkv, r, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=off + 3, row_out=gv["dqkv"][0],
+            if self.time_standin:
+                ev[1].record()
+                self._standin_events.append(ev)
+            fp4_quantize(self.dqkv, r, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=off3, row_out=gv["dqkv"][0],
                          col_out=gv["dqkv"][1], workspace=self.ws)
             fp4_linear_wgrad(gv["dqkv"][1], s["y1"][1], dw["qkv"])
             fp4_linear_dgrad_rmsnorm(gv["dqkv"][0], wv["qkv"][1], s["r1"], s["rstd1"], self.g1, dx=self.dy,
@@ -200,12 +224,24 @@ class FP4LinearStack:
             dF = self.gviews[prev_route]["dF"] if i > 0 else self.views_in[r]
             dr1 = self.dr1[i % 2]  # never the buffer that holds dh_out (block i + 1's)
             fp4_residual_rmsnorm_bwd_parts(self.dy, self.part, s["r1"], s["rstd1"], self.g1, dr2, prev_route,
-                                           3 if i > 0 else FP4_VIEW_ROW, True, sr_seed, off + 4, dr=dr1,
+                                           3 if i > 0 else FP4_VIEW_ROW, True, sr_seed, off4, dr=dr1,
                                            dr_row=dF[0], dr_col=dF[1] if i > 0 else None, workspace=self.ws)
             dh_out = dr1
         return dh_out
 
     def step(self, x: torch.Tensor, dy: torch.Tensor, sr_seed: int = 1):
+        """One forward + backward; the step index advances, so the next
+        step's stochastic rounding draws fresh random numbers."""
         self.quantize_weights()
         self.forward(x)
-        return self.backward(dy, sr_seed)
+        out = self.backward(dy, sr_seed, self.step_index)
+        self.step_index += 1
+        return out
+
+    def standin_ms(self) -> float:
+        """Device milliseconds of the attention stand-in's copies recorded
+        since the last call (time_standin must be set); synchronises."""
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in self._standin_events)
+        self._standin_events = []
+        return ms
