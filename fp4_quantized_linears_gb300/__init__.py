@@ -123,6 +123,8 @@ def _declare(L):
                                             ctypes.c_int, ctypes.c_int, c_u64, c_u64, vp, tp, tp, vp, c_sz, vp]),
         "fp4_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_int)]),
         "fp4_status_reset": (ctypes.c_int, [vp]),
+        "fp4_set_wait_limit": (ctypes.c_int, [c_u64]),
+        "fp4_test_skip_accumulator_release": (ctypes.c_int, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -514,6 +516,18 @@ def fp4_status(stream=None) -> int:
 
 def fp4_status_reset(stream=None):
     _check(load().fp4_status_reset(_stream(stream)), "fp4_status_reset")
+
+
+def fp4_set_wait_limit(cycles: int = 0):
+    """Bound (SM clock cycles) of the GEMM kernels' barrier waits for the
+    launches that follow; 0 restores the default."""
+    _check(load().fp4_set_wait_limit(int(cycles)), "fp4_set_wait_limit")
+
+
+def fp4_test_skip_accumulator_release(enable: bool):
+    """Test hook: the following GEMM launches skip their first accumulator
+    release, so a bounded wait runs out and reports FP4_ERR_TIMEOUT."""
+    _check(load().fp4_test_skip_accumulator_release(1 if enable else 0), "fp4_test_skip_accumulator_release")
 
 
 def fp4_version() -> int:

@@ -9,6 +9,7 @@
 
 #include <mutex>
 
+#include "common.cuh"
 #include "internal.h"
 
 using namespace fp4;
@@ -67,6 +68,7 @@ int fp4_quantize_workspace_bytes(int route, int64_t rows, int64_t cols, unsigned
 int fp4_quantize_hybrid_workspace_bytes(int row_route, int col_route, int64_t rows, int64_t cols, unsigned views,
                                         unsigned flags, size_t* bytes) {
     if (!route_ok(row_route) || !route_ok(col_route) || !bytes || rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;
+    if ((views & ~3u) || (flags & ~15u)) return FP4_ERR_INVALID_ARG;
     if (rows % 128 || cols % 128) return FP4_ERR_UNSUPPORTED_SHAPE;
     *bytes = quant_workspace_slots(rows, cols, row_route, col_route, views ? views : 3u, flags) * 4;
     return FP4_OK;
@@ -129,6 +131,7 @@ static int prepare_quant(const void* x, bool x_from_pre, int64_t rows, int64_t c
     p->flags = flags;
     p->seed = sr_seed;
     p->offset = sr_offset;
+    sr_round_keys(sr_seed, p->sr_keys);
     p->sign_mask = sign_mask;
     if (do_row) {
         p->row_codes = static_cast<uint8_t*>(row_out->codes);
@@ -547,6 +550,20 @@ int fp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld, 
     size_t need = 0;
     int rc = fp4_quantize_workspace_bytes(route, rows, cols, views, flags, &need);
     if (rc != FP4_OK) return rc;
+    // Every argument check of fp4_quantize comes first (on copies of the
+    // views, with a stand-in workspace of the needed size that is never
+    // touched), so an invalid call fails the same way as there; only then is
+    // the shape held against the scratch array's size.
+    {
+        fp4_tensor r_chk = row_out ? *row_out : fp4_tensor{};
+        fp4_tensor c_chk = col_out ? *col_out : fp4_tensor{};
+        QuantParams chk;
+        static uint32_t stand_in;
+        rc = prepare_quant(x, false, rows, cols, ld, route, route, views, flags, sr_seed, sr_offset, hadamard_signs,
+                           row_out ? &r_chk : nullptr, col_out ? &c_chk : nullptr, need ? &stand_in : nullptr, need,
+                           &chk);
+        if (rc != FP4_OK) return rc;
+    }
     if (need > FP4_NOALLOC_SCRATCH_BYTES) return FP4_ERR_WORKSPACE;
     void* ws = nullptr;
     if (need > 0 && rows > 0 && cols > 0) {
@@ -564,6 +581,16 @@ int fp4_status(fp4_stream_t stream, int* code) {
     if ((r = quant_status(s, &a, false)) != FP4_OK) return r;
     if ((r = gemm_status(s, &b, false)) != FP4_OK) return r;
     *code = a ? a : b;
+    return FP4_OK;
+}
+
+int fp4_set_wait_limit(uint64_t cycles) {
+    gemm_set_wait_limit(cycles);
+    return FP4_OK;
+}
+
+int fp4_test_skip_accumulator_release(int enable) {
+    gemm_test_skip_first_release(enable);
     return FP4_OK;
 }
 

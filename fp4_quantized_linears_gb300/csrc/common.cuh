@@ -46,6 +46,22 @@ FP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
     return r;
 }
 
+// Eight binary32 values -> one word of eight E2M1 codes (value 2k in the low
+// nibble of byte k), four conversions assembled into the word by one vector
+// move; the same rounding as e2m1x2_rn.
+FP4_DEV uint32_t e2m1x8_rn(float a0, float a1, float a2, float a3, float a4, float a5, float a6, float a7) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+    return r;
+}
+
 // ----------------------------------------------------- packed binary32 ----
 // Two binary32 lanes per instruction (f32x2 arithmetic of sm_100 and later):
 // each lane is the correctly rounded result of the scalar operation on
@@ -102,13 +118,21 @@ FP4_DEV float max3_abs_nan(float m, float a, float b) {
 // sr_code_pair takes the two scaled magnitudes and returns their two 3-bit
 // magnitude codes (x in the low nibble); rw holds u_x in its low and u_y in
 // its high 16 bits.
+// SAT: saturate at code 7 (|v| >= 6).  Without it the caller guarantees
+// |v| <= 6, as an MXFP4 block under its upward scale does (6 * 2^e >= amax,
+// and scaling by 2^-e is exact); then b <= 6 and the code is at most 7.
+template <bool SAT = true>
 FP4_DEV uint32_t sr_code_pair(float ax, float ay, uint32_t rw) {
     float cx, cy;
     f32x2_fma_rp(cx, cy, ax, ay, 0.5f, 0.5f, 0.5f, 0.5f);  // fl_up((|v| + 1) / 2)
     const uint32_t tx = max(__float_as_uint(ax), __float_as_uint(cx));
     const uint32_t ty = max(__float_as_uint(ay), __float_as_uint(cy));
-    const uint32_t hx = min((tx + (((rw << 6) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
-    const uint32_t hy = min((ty + (((rw >> 10) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22, 7u);
+    uint32_t hx = (tx + (((rw << 6) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22;
+    uint32_t hy = (ty + (((rw >> 10) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22;
+    if (SAT) {
+        hx = min(hx, 7u);
+        hy = min(hy, 7u);
+    }
     return hx | (hy << 4);
 }
 FP4_DEV uint32_t e2m1x2_sr(float x, float y, uint32_t rw) {
@@ -118,11 +142,12 @@ FP4_DEV uint32_t e2m1x2_sr(float x, float y, uint32_t rw) {
 // The two bf16 values of one word (low half first) scaled by a non-negative
 // multiplier (fl32(x * mult), as the RN path) and rounded stochastically; the
 // codes keep the inputs' sign bits.
+template <bool SAT = true>
 FP4_DEV uint32_t e2m1x2_sr_bf16(uint32_t w, float mult, uint32_t rw) {
     const uint32_t wa = w & 0x7FFF7FFFu;
     float ax, ay;
     f32x2_mul(ax, ay, __uint_as_float(wa << 16), __uint_as_float(wa & 0xFFFF0000u), mult, mult);
-    return sr_code_pair(ax, ay, rw) | ((w >> 12) & 8u) | ((w >> 24) & 0x80u);
+    return sr_code_pair<SAT>(ax, ay, rw) | ((w >> 12) & 8u) | ((w >> 24) & 0x80u);
 }
 
 // --------------------------------------------------------------- E4M3 ------
@@ -176,23 +201,34 @@ FP4_DEV uint32_t nv_block_scale(float block_amax, float senc, float& mult) {
 
 // -------------------------------------------------------------- Philox ----
 // Philox4x32-10: ten rounds of the 4x32 S-box with key increments.  Each
-// round's two 32x32 -> 64-bit products are single widening multiplies.
-FP4_DEV uint4 philox4x32_10(uint4 c, uint2 k) {
+// round's two 32x32 -> 64-bit products are single widening multiplies.  The
+// ten round keys depend only on the seed: the host computes them once per
+// launch (sr_round_keys) and the kernels read them from their parameters.
+constexpr int SR_ROUND_KEYS = 20;
+__host__ __device__ inline void sr_round_keys(uint64_t seed, uint32_t* rk) {
+    uint32_t kx = (uint32_t)seed, ky = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        rk[2 * r] = kx;
+        rk[2 * r + 1] = ky;
+        kx += 0x9E3779B9u;
+        ky += 0xBB67AE85u;
+    }
+}
+FP4_DEV uint4 philox4x32_10(uint4 c, const uint32_t* rk) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
         const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
-        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.x, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k.y, (uint32_t)p0);
-        k.x += 0x9E3779B9u;
-        k.y += 0xBB67AE85u;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk[2 * r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ rk[2 * r + 1],
+                       (uint32_t)p0);
     }
     return c;
 }
 
-// The eight 16-bit uniforms of elements 8g .. 8g+7 under (seed, offset).
-FP4_DEV uint4 sr_bits8(uint64_t g, uint64_t seed, uint64_t offset) {
-    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
-                         make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+// The eight 16-bit uniforms of elements 8g .. 8g+7 under (seed, offset); rk
+// holds the seed's round keys.
+FP4_DEV uint4 sr_bits8(uint64_t g, const uint32_t* rk, uint64_t offset) {
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)), rk);
 }
 
 // ----------------------------------------------------------- scale layout --

@@ -53,6 +53,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -73,8 +74,8 @@ constexpr int EPI_WARPS = 8;  // epilogue warps (16 for the SwiGLU backward; war
 constexpr int SF_WARPS = 2;   // after the epilogue warps: each copies every SF_WARPS-th scale chunk of a stage
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;  // first TMEM column of the scale-factor region
-constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
-constexpr int GROUP_M = 8;     // raster: 8 M-units per band
+constexpr long long WAIT_CYCLES = 4000000000LL;  // default wait bound, ~2 s at 2 GHz
+constexpr int64_t L2_RESIDENT_BYTES = 40ll << 20;  // raster: budget for the operand kept in L2
 
 // ------------------------------------------------------------ PTX wrappers -
 FP4_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -109,12 +110,12 @@ FP4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait; false (and the status word set) when the budget runs out.
-FP4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait; false (and the status word set) when `limit` cycles pass.
+FP4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > WAIT_CYCLES) {
+        if (clock64() - t0 > limit) {
             set_status(&g_status_gemm, FP4_ERR_TIMEOUT);
             return false;
         }
@@ -173,6 +174,12 @@ FP4_DEV void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, i
                  : "memory");
 }
 FP4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// 16-byte asynchronous global -> shared copy (L2 only) and its completion
+FP4_DEV void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+FP4_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+FP4_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // at most N committed bulk groups may still be reading their shared source
 template <int N>
 FP4_DEV void bulk_wait_read() {
@@ -402,15 +409,10 @@ FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
+        float s8[8];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            int i = q * 8 + b * 2;
-            float x, y;
-            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
-            word |= e2m1x2_rn(x, y) << (8 * b);
-        }
-        w[q] = word;
+        for (int b = 0; b < 8; b += 2) f32x2_mul(s8[b], s8[b + 1], v[q * 8 + b], v[q * 8 + b + 1], mult, mult);
+        w[q] = e2m1x8_rn(s8[0], s8[1], s8[2], s8[3], s8[4], s8[5], s8[6], s8[7]);
     }
     packed = make_uint4(w[0], w[1], w[2], w[3]);
     return (uint32_t)(e + 127);
@@ -423,7 +425,7 @@ FP4_DEV uint32_t lanes_max_f32bits(uint32_t m2) { return max(m2 << 16, m2 & 0xFF
 // stochastic rounding: scale byte and 16 bytes of codes.  The block maximum
 // is taken on the bf16 magnitudes (their unsigned order is the numeric one;
 // a NaN still ends at or above the infinity pattern).
-FP4_DEV uint32_t mx_words_sr(const uint32_t* w, uint64_t g0, uint64_t seed, uint64_t offset, uint4& packed) {
+FP4_DEV uint32_t mx_words_sr(const uint32_t* w, uint64_t g0, const uint32_t* rk, uint64_t offset, uint4& packed) {
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
@@ -434,11 +436,11 @@ FP4_DEV uint32_t mx_words_sr(const uint32_t* w, uint64_t g0, uint64_t seed, uint
     uint32_t out[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint4 rb = sr_bits8(g0 + q, seed, offset);
+        const uint4 rb = sr_bits8(g0 + q, rk, offset);
         const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
         uint32_t word = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16(w[4 * q + b], mult, rw[b]) << (8 * b);
+        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16<false>(w[4 * q + b], mult, rw[b]) << (8 * b);
         out[q] = word;
     }
     packed = make_uint4(out[0], out[1], out[2], out[3]);
@@ -454,16 +456,14 @@ FP4_DEV uint32_t mx_lane_rn(const uint32_t* w, int h, uint32_t am, uint4& packed
     uint32_t out[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
+        float s8[8];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int i = q * 8 + b * 2;
-            float x, y;
-            f32x2_mul(x, y, h ? bf16_hi(w[i]) : bf16_lo(w[i]), h ? bf16_hi(w[i + 1]) : bf16_lo(w[i + 1]), mult,
-                      mult);
-            word |= e2m1x2_rn(x, y) << (8 * b);
+        for (int b = 0; b < 8; b += 2) {
+            const int i = q * 8 + b;
+            f32x2_mul(s8[b], s8[b + 1], h ? bf16_hi(w[i]) : bf16_lo(w[i]), h ? bf16_hi(w[i + 1]) : bf16_lo(w[i + 1]),
+                      mult, mult);
         }
-        out[q] = word;
+        out[q] = e2m1x8_rn(s8[0], s8[1], s8[2], s8[3], s8[4], s8[5], s8[6], s8[7]);
     }
     packed = make_uint4(out[0], out[1], out[2], out[3]);
     return (uint32_t)(e + 127);
@@ -527,6 +527,7 @@ struct KParams {
     uint8_t* q_col_codes;  // fwd: Q_c(h) [f][M];   bwd: Q_c(da13) [2f][M]
     uint8_t* q_col_scales;
     uint64_t seed, offset;
+    uint32_t sr_keys[SR_ROUND_KEYS];  // Philox round keys of `seed`
     // QKV producer with RoPE: head-major bf16 outputs [heads][M][128]
     uint16_t* q_out;
     uint16_t* k_out;
@@ -540,6 +541,13 @@ struct KParams {
     const uint16_t* rms_g;
     const float* rms_rstd;
     float* rms_part;
+    long long wait_cycles;   // bound of every mbarrier wait
+    int skip_first_release;  // test hook: the epilogue's first accumulator release is skipped
+    // raster: bands of `band` units along M (n_inner = 0: M fastest inside a
+    // band, the band's A tiles reused from L2 while B streams) or along N
+    // (n_inner = 1: N fastest, the band's B tiles reused while A streams)
+    int n_inner;
+    int64_t band;
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -574,10 +582,14 @@ struct Cfg {
     static constexpr int OUT_BOX = 32 * OUT_ROW;
     static constexpr int OUT_BUFS =
         !is_store(EPI) ? 0 : (fit(EPI_WARPS * 2 * OUT_BOX) >= MAX_STAGES_OUT ? 2 : 1);
+    // SwiGLU backward on CTA pairs: each epilogue thread's retained a1 / a3
+    // row segments (2 x 64 bytes) of the next tile land in a slot of its own
+    static constexpr bool BWD_PREFETCH = EPI == EPI_SWIGLU_BWD && P2;
+    static constexpr int PREFETCH_BYTES = BWD_PREFETCH ? epi_warps(EPI) * 32 * 128 : 0;
     static constexpr int STAGING =
         is_store(EPI)         ? EPI_WARPS * OUT_BUFS * OUT_BOX
         : EPI == EPI_QKV_ROPE ? 0
-                              : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512;
+                              : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512 + PREFETCH_BYTES;
     static constexpr int STAGES = fit(STAGING);
     static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + RESERVED;
     static_assert(STAGES >= 3, "pipeline depth");
@@ -590,7 +602,7 @@ template <bool NV, int BN, int EPI, int CM, bool P2 = false>
 __global__ void __launch_bounds__(kthreads(EPI), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
-                    const __grid_constant__ CUtensorMap tmSB, KParams p) {
+                    const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ KParams p) {
     using C = Cfg<NV, BN, EPI, P2>;
     static_assert(P2 ? CM == 2 : CM == 1, "clusters are CTA pairs");
     static_assert(!P2 || BN == 256 || EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD, "pair tile widths");
@@ -623,6 +635,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = CM > 1 ? cluster_rank() : 0;
+    const long long lim = p.wait_cycles;
     const int num_kb = (int)(p.K / BK);
     const int64_t m_units = p.M / (BM * CM);
     const int64_t n_blocks = EPI == EPI_SWIGLU_FWD ? p.f / 128 : p.N / BN;
@@ -630,12 +643,22 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
     const int64_t cluster_id = blockIdx.x / CM, n_clusters = gridDim.x / CM;
 
     auto unit_coords = [&](int64_t u, int64_t& m0, int64_t& n0) {
-        const int64_t per_group = (int64_t)GROUP_M * n_blocks;
-        const int64_t g = u / per_group, within = u % per_group;
-        const int64_t m_first = g * GROUP_M;
-        const int64_t gs = min((int64_t)GROUP_M, m_units - m_first);
-        const int64_t mu = m_first + within % gs;
-        const int64_t nb = within / gs;
+        int64_t mu, nb;
+        if (p.n_inner) {
+            const int64_t per_group = p.band * m_units;
+            const int64_t g = u / per_group, within = u % per_group;
+            const int64_t n_first = g * p.band;
+            const int64_t gs = min(p.band, n_blocks - n_first);
+            nb = n_first + within % gs;
+            mu = within / gs;
+        } else {
+            const int64_t per_group = p.band * n_blocks;
+            const int64_t g = u / per_group, within = u % per_group;
+            const int64_t m_first = g * p.band;
+            const int64_t gs = min(p.band, m_units - m_first);
+            mu = m_first + within % gs;
+            nb = within / gs;
+        }
         m0 = (mu * CM + rank) * BM;
         n0 = nb * (EPI == EPI_SWIGLU_FWD ? 128 : BN);
     };
@@ -704,7 +727,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
             int64_t m0, n0;
             unit_coords(u, m0, n0);
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) {
+                if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, lim)) {
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -751,9 +774,10 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 }
             }
         }
-        if (!ok && (!P2 || rank == 0)) {
+        if ((!ok || *abort_flag) && (!P2 || rank == 0)) {
             // drain: wait (bounded) for the loads of the stages still in flight
-            // (pair: the leader's barriers count the loads of both CTAs)
+            // when this or another role gave up (pair: the leader's barriers
+            // count the loads of both CTAs)
             int s = stage;
             uint32_t ph = phase;
             for (int i = 0; i < STAGES && i < issued; ++i) {
@@ -761,7 +785,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     s = STAGES - 1;
                     ph ^= 1;
                 }
-                mbar_wait(&full[s], ph);
+                mbar_wait(&full[s], ph, lim);
             }
         }
     } else if (warp == 1 && lane == 0 && (!P2 || rank == 0)) {
@@ -772,7 +796,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true;
         for (int64_t u = cluster_id; u < n_units && ok; u += n_clusters) {
-            if (*abort_flag || !mbar_wait(acc_empty, acc_phase ^ 1)) {
+            if (*abort_flag || !mbar_wait(acc_empty, acc_phase ^ 1, lim)) {
                 *abort_flag = 1;
                 ok = false;
                 break;
@@ -780,7 +804,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
             tc_fence_after();
             for (int kb = 0; kb < num_kb; ++kb) {
                 // the stage has landed and its scale factors are in TMEM
-                if (*abort_flag || !mbar_wait(&sf_full[stage], phase)) {
+                if (*abort_flag || !mbar_wait(&sf_full[stage], phase, lim)) {
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -828,7 +852,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         // drain point of everything issued (its own barrier, so that no
         // epilogue wait on acc_full can see an extra phase)
         tc_commit<G>(drain_bar);
-        mbar_wait(drain_bar, 0);
+        mbar_wait(drain_bar, 0, lim);
     } else if (warp >= SF_WARP && lane == 0 && (!P2 || rank == 0)) {
         // ------------------------------------------------ scale factors ---
         // Each landed stage's scale atoms go to that stage's TMEM columns
@@ -849,7 +873,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         bool ok = true;
         for (int64_t u = cluster_id; u < n_units && ok; u += n_clusters) {
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (*abort_flag || !mbar_wait(&full[stage], phase)) {
+                if (*abort_flag || !mbar_wait(&full[stage], phase, lim)) {
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -876,7 +900,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         }
         // every copy issued has completed before TMEM can be released
         tc_commit<G>(sf_drain);
-        mbar_wait(sf_drain, 0);
+        mbar_wait(sf_drain, 0, lim);
     } else if (warp >= 2 && warp < 2 + EW) {
         // ------------------------------------------------ epilogue --------
         const int q = warp & 3;               // TMEM lane quarter this warp may access
@@ -885,10 +909,15 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         const int et = (warp - 2) * 32 + lane;  // epilogue thread index 0 .. 32 * EW - 1
         uint32_t acc_phase = 0, epi_phase = 0;
         bool epi_ok = true;
+        bool skip_release = p.skip_first_release != 0;  // test hook, first tile only
         // the accumulator is free once every epilogue warp has read it; in
         // pair mode the MMA thread waits on the leader's barrier for the
         // warps of both CTAs
         auto release_acc = [&]() {
+            if (skip_release) {
+                skip_release = false;
+                return;
+            }
             if (lane == 0) {
                 if (P2 && rank != 0)
                     mbar_arrive_cluster(mapa_rank(smem_u32(acc_empty), 0));
@@ -901,16 +930,36 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         auto epi_sync = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(epi_bar);
-            if (!mbar_wait(epi_bar, epi_phase)) {
+            if (!mbar_wait(epi_bar, epi_phase, lim)) {
                 *abort_flag = 1;
                 epi_ok = false;
             }
             epi_phase ^= 1;
         };
+        // SwiGLU backward (pairs): this thread's a1 / a3 row segments of a
+        // tile are copied into its own shared slot one tile ahead, so that
+        // their latency hides behind the previous tile's work
+        const uint32_t slot = smem_u32(staging + 2 * BM * ST_LDS * 2 + 4 * 512) + (uint32_t)et * 128;
+        auto prefetch_a13 = [&](int64_t u2) {
+            if constexpr (C::BWD_PREFETCH) {
+                if (u2 < n_units) {
+                    int64_t m2, n2;
+                    unit_coords(u2, m2, n2);
+                    const int64_t off = (m2 + lr) * p.f + n2 + 32 * half;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        cp_async16(slot + 16 * i, p.a1 + off + 8 * i);
+                        cp_async16(slot + 64 + 16 * i, p.a3 + off + 8 * i);
+                    }
+                }
+                cp_async_commit();
+            }
+        };
+        prefetch_a13(cluster_id);
         for (int64_t u = cluster_id; u < n_units && epi_ok; u += n_clusters) {
             int64_t m0, n0;
             unit_coords(u, m0, n0);
-            if constexpr (EPI == EPI_SWIGLU_BWD) {
+            if constexpr (EPI == EPI_SWIGLU_BWD && !C::BWD_PREFETCH) {
                 // this thread's retained a1 / a3 (one 64-byte row segment
                 // each) do not depend on the accumulator: start moving them
                 // into L2 while the tile's MMAs run
@@ -918,7 +967,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 bulk_prefetch_l2(p.a1 + off, 64);
                 bulk_prefetch_l2(p.a3 + off, 64);
             }
-            if (!mbar_wait(acc_full, acc_phase)) {
+            if (!mbar_wait(acc_full, acc_phase, lim)) {
                 *abort_flag = 1;
                 break;
             }
@@ -1231,13 +1280,24 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 // da1 = bf16(dh * a3 * SiLU'(a1)), da3 = bf16(dh * SiLU(a1)), as bf16x2 words
                 uint32_t q1[16], q3[16];
                 {
-                    const uint4* pa1 = reinterpret_cast<const uint4*>(p.a1 + m * p.f + n);
-                    const uint4* pa3 = reinterpret_cast<const uint4*>(p.a3 + m * p.f + n);
                     uint4 v1[4], v3[4];
+                    if constexpr (C::BWD_PREFETCH) {
+                        cp_async_wait_all();  // this thread's own copies of this tile's segments
+                        const uint4* s13 = reinterpret_cast<const uint4*>(staging + 2 * BM * ST_LDS * 2 + 4 * 512 +
+                                                                          et * 128);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        v1[i] = pa1[i];
-                        v3[i] = pa3[i];
+                        for (int i = 0; i < 4; ++i) {
+                            v1[i] = s13[i];
+                            v3[i] = s13[4 + i];
+                        }
+                    } else {
+                        const uint4* pa1 = reinterpret_cast<const uint4*>(p.a1 + m * p.f + n);
+                        const uint4* pa3 = reinterpret_cast<const uint4*>(p.a3 + m * p.f + n);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            v1[i] = pa1[i];
+                            v3[i] = pa3[i];
+                        }
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -1262,6 +1322,8 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                         }
                     }
                 }
+                // the slot's values are consumed: the next tile's segments may land
+                prefetch_a13(u + n_clusters);
                 if (p.tap1) {
                     store_words16(p.tap1 + m * f2 + n, q1);
                     store_words16(p.tap1 + m * f2 + p.f + n, q3);
@@ -1269,10 +1331,10 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 if (p.quantize) {
                     // row views of [da1 | da3] (stochastic rounding), one block each
                     uint4 pk;
-                    uint32_t sc = mx_words_sr(q1, (uint64_t)(m * f2 + n) >> 3, p.seed, p.offset, pk);
+                    uint32_t sc = mx_words_sr(q1, (uint64_t)(m * f2 + n) >> 3, p.sr_keys, p.offset, pk);
                     *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + (n >> 1)) = pk;
                     atoms[atom_off(lr, half)] = (uint8_t)sc;
-                    sc = mx_words_sr(q3, (uint64_t)(m * f2 + p.f + n) >> 3, p.seed, p.offset, pk);
+                    sc = mx_words_sr(q3, (uint64_t)(m * f2 + p.f + n) >> 3, p.sr_keys, p.offset, pk);
                     *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + ((p.f + n) >> 1)) = pk;
                     atoms[512 + atom_off(lr, half)] = (uint8_t)sc;
                     store_words16(s1 + lr * ST_LDS + oc, q1);
@@ -1322,6 +1384,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         }
     }
     if (is_store(EPI) && warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores done with shared memory
+    if (Cfg<NV, BN, EPI, P2>::BWD_PREFETCH && warp >= 2 && warp < 2 + EW) cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
     if (CM > 1) cluster_sync();  // the peer no longer arrives on this CTA's barriers
@@ -1459,7 +1522,21 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
     }
     const int64_t clusters = n_units < max_clusters ? n_units : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * CM));
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsa, tsb, kp) != cudaSuccess) return FP4_ERR_CUDA;
+    // Raster: the operand with fewer code bytes stays in L2 (a band of its
+    // tiles as wide as the budget allows, all of it when it fits) while the
+    // other streams through once per band.
+    KParams k = kp;
+    {
+        const int64_t m_units = g.M / (BM * CM);
+        const int64_t n_blocks = EPI == EPI_SWIGLU_FWD ? g.f / 128 : g.N / BN;
+        const int64_t a_unit = (int64_t)BM * CM * (g.K / 2), b_unit = (int64_t)(EPI == EPI_SWIGLU_FWD ? 256 : BN) * (g.K / 2);
+        const bool n_inner = b_unit * n_blocks < a_unit * m_units;
+        const int64_t unit_bytes = n_inner ? b_unit : a_unit, units = n_inner ? n_blocks : m_units;
+        int64_t band = L2_RESIDENT_BYTES / (unit_bytes > 0 ? unit_bytes : 1);
+        k.n_inner = n_inner ? 1 : 0;
+        k.band = band < 1 ? 1 : (band > units ? units : band);
+    }
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsa, tsb, k) != cudaSuccess) return FP4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -1489,6 +1566,7 @@ KParams kparams_of(const GemmParams& g) {
     p.q_col_scales = g.q_col_scales;
     p.seed = g.seed;
     p.offset = g.offset;
+    sr_round_keys(g.seed, p.sr_keys);
     p.q_out = g.q_out;
     p.k_out = g.k_out;
     p.v_out = g.v_out;
@@ -1506,11 +1584,16 @@ KParams kparams_of(const GemmParams& g) {
 
 }  // namespace
 
+std::atomic<long long> g_wait_cycles{WAIT_CYCLES};
+std::atomic<int> g_skip_first_release{0};
+
 int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     if (!get_encode()) return FP4_ERR_CUDA;
     GemmParams g = g0;
     const bool pair = (g.M / BM) % 2 == 0;
-    const KParams kp = kparams_of(g);
+    KParams kp = kparams_of(g);
+    kp.wait_cycles = g_wait_cycles.load();
+    kp.skip_first_release = g_skip_first_release.load();
     if (g.epi == 1) {  // SwiGLU forward: B = [W1; W3] with 2f rows, output width f
         g.b_rows = 2 * g.f;
         const int64_t units_1 = (g.M / BM) * (g.f / 128);
@@ -1556,6 +1639,11 @@ int launch_gemm(const GemmParams& g0, cudaStream_t stream) {
     return pair ? launch_t<false, 128, EPI_STORE, 2, true>(g, kp, units_1 / 2, stream)
                 : launch_t<false, 128, EPI_STORE, 1>(g, kp, units_1, stream);
 }
+
+void gemm_set_wait_limit(uint64_t cycles) {
+    g_wait_cycles.store(cycles == 0 || cycles > (uint64_t)WAIT_CYCLES * 1000 ? WAIT_CYCLES : (long long)cycles);
+}
+void gemm_test_skip_first_release(int enable) { g_skip_first_release.store(enable ? 1 : 0); }
 
 int gemm_status(cudaStream_t stream, int* code, bool reset) {
     unsigned int v = 0;

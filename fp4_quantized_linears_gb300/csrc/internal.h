@@ -15,6 +15,7 @@ struct QuantParams {
     int row_route, col_route;  // FP4_ROUTE_* of each view (they differ in the operand-wise hybrid)
     unsigned views, flags;
     uint64_t seed, offset;
+    uint32_t sr_keys[20];  // Philox round keys of `seed` (sr_round_keys)
     uint32_t sign_mask;  // bit j set: sign j of the H32 / H16 diagonal is -1
     uint8_t* row_codes;
     uint8_t* row_scales;
@@ -108,5 +109,7 @@ struct GemmParams {
 
 int launch_gemm(const GemmParams& p, cudaStream_t stream);
 int gemm_status(cudaStream_t stream, int* code, bool reset);
+void gemm_set_wait_limit(uint64_t cycles);     // 0: the default bound
+void gemm_test_skip_first_release(int enable);  // test hook (fp4_test_skip_accumulator_release)
 
 }  // namespace fp4

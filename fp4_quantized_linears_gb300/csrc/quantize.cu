@@ -89,32 +89,29 @@ FP4_DEV uint4 pack_rn32(const float* v, float m0, float m1) {
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        float mult = q < 2 ? m0 : m1;
-        uint32_t word = 0;
+        const float mult = q < 2 ? m0 : m1;
+        float s[8];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            int i = q * 8 + b * 2;
-            float x, y;
-            f32x2_mul(x, y, v[i], v[i + 1], mult, mult);
-            word |= e2m1x2_rn(x, y) << (8 * b);
-        }
-        w[q] = word;
+        for (int b = 0; b < 8; b += 2) f32x2_mul(s[b], s[b + 1], v[q * 8 + b], v[q * 8 + b + 1], mult, mult);
+        w[q] = e2m1x8_rn(s[0], s[1], s[2], s[3], s[4], s[5], s[6], s[7]);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Stochastic rounding of the 32 bf16 values of 16 words (logical indices
-// 8*g0 .. 8*g0+31), scaled by m0 (values 0..15) and m1 (16..31).
-FP4_DEV uint4 pack_sr32(const uint32_t* w, float m0, float m1, uint64_t g0, uint64_t seed, uint64_t offset) {
+// 8*g0 .. 8*g0+31), scaled by m0 (values 0..15) and m1 (16..31); SAT for
+// NVFP4 blocks, whose scaled values can pass 6 by the E4M3 scale rounding.
+template <bool SAT>
+FP4_DEV uint4 pack_sr32(const uint32_t* w, float m0, float m1, uint64_t g0, const uint32_t* rk, uint64_t offset) {
     uint32_t out[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint4 rb = sr_bits8(g0 + q, seed, offset);
+        const uint4 rb = sr_bits8(g0 + q, rk, offset);
         const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
         const float mult = q < 2 ? m0 : m1;
         uint32_t word = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16(w[4 * q + b], mult, rw[b]) << (8 * b);
+        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16<SAT>(w[4 * q + b], mult, rw[b]) << (8 * b);
         out[q] = word;
     }
     return make_uint4(out[0], out[1], out[2], out[3]);
@@ -442,7 +439,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             uint4 packed;
             if (sr) {
                 const uint64_t g0 = (uint64_t)(((r0 + r) * p.C + c0 + 32 * j) >> 3);
-                packed = pack_sr32(w, m0, m1, g0, p.seed, p.offset);
+                packed = pack_sr32<NVR>(w, m0, m1, g0, p.sr_keys, p.offset);
             } else {
                 float v[32];
 #pragma unroll
@@ -576,7 +573,7 @@ FP4_DEV void prefetch_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_
 // already in flight, so its load latency hides behind the encoding.  With an
 // RMSNorm pre-op the tile is loaded (and transformed) synchronously.
 template <bool NVR, bool NVC>
-__global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p) {
+__global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(const __grid_constant__ QuantParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
     const int64_t tiles_x = p.C / TILE, n_tiles = tiles_x * (p.R / TILE);
@@ -609,7 +606,7 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(QuantParams p
 // When the column view is NVFP4 through H16, its factors are those of the
 // transformed values: the column-strip slots and the last slot (the global
 // column factor) then take the maxima of the H16 output of each 16-row block.
-__global__ void __launch_bounds__(THREADS) nv_amax_kernel(QuantParams p) {
+__global__ void __launch_bounds__(THREADS) nv_amax_kernel(const __grid_constant__ QuantParams p) {
     __shared__ uint32_t red[2][THREADS / 32];
     extern __shared__ __align__(16) uint8_t amax_smem[];
     uint16_t* tile = reinterpret_cast<uint16_t*>(amax_smem);

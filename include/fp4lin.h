@@ -382,6 +382,22 @@ FP4_API int fp4_status(fp4_stream_t stream, int* code);
 /* Clear the sticky device status word (enqueued on `stream`). */
 FP4_API int fp4_status_reset(fp4_stream_t stream);
 
+/* Bound of every mbarrier wait in the GEMM kernels, in SM clock cycles, for
+ * the launches that follow this call (process-wide).  A wait that runs out
+ * sets FP4_ERR_TIMEOUT in the status word; the kernel then waits (again
+ * bounded) for the copies it issued, releases its tensor memory and returns,
+ * so the context stays usable.  cycles = 0 restores the default (4e9, about
+ * 2 s at 2 GHz).  Host only; returns FP4_OK. */
+FP4_API int fp4_set_wait_limit(uint64_t cycles);
+
+/* Test hook for the timeout path above: with enable != 0, the GEMM launches
+ * that follow skip their epilogue's first accumulator release, so the MMA
+ * thread's next wait for the accumulator cannot be satisfied and runs out
+ * after the wait limit (a barrier that no copy targets; nothing faults).
+ * enable = 0 restores normal operation.  Not for production use; results of
+ * launches made while it is set are invalid.  Host only; returns FP4_OK. */
+FP4_API int fp4_test_skip_accumulator_release(int enable);
+
 #ifdef __cplusplus
 }
 #endif

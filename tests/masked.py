@@ -13,6 +13,7 @@ is test code, not the oracle)."""
 import numpy as np
 
 from layout import expand_outer, unpack_codes, unswizzle_scales
+from parity_stats import record
 
 E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
 
@@ -62,10 +63,13 @@ def _step(a: np.ndarray) -> np.ndarray:
 
 
 def assert_view_masked(got: dict, want: dict, gpu_vals: np.ndarray, same_vals: np.ndarray, what: str,
-                       max_bad_frac: float = 0.05):
+                       max_bad_frac: float = 0.004):
     """got/want: host views (GPU / oracle) of one orientation; gpu_vals and
     same_vals: the GPU's BF16 inputs of that view and the element mask where
-    they equal the oracle's, both [rows, cols] in the view's orientation."""
+    they equal the oracle's, both [rows, cols] in the view's orientation.
+    max_bad_frac: at most 0.4 % of the scale blocks may have inputs that
+    differ from the oracle's (about twice the largest fraction observed on
+    any of the seeded workloads, 0.195 %)."""
     bs = want["bs"]
     rows, cols = want["codes"].shape
     ok = same_vals.reshape(rows, cols // bs, bs).all(2)
@@ -75,6 +79,7 @@ def assert_view_masked(got: dict, want: dict, gpu_vals: np.ndarray, same_vals: n
         same_outer = np.asarray(got["senc"]) == np.asarray(want["senc"])
         ok &= same_outer[:, None]
     bad_frac = 1.0 - ok.mean()
+    record(what, masked_block_frac=bad_frac)
     assert bad_frac <= max_bad_frac, f"{what}: {bad_frac:.2%} of blocks differ in their inputs"
     okm = np.repeat(ok, bs, axis=1)
     nc = int(np.sum((got["codes"] != want["codes"]) & okm))

@@ -123,3 +123,30 @@ def test_dgrad_rmsnorm_validation_codes():
     # shape rule of the RMSNorm backward
     assert r(0, 3, 1, ok16, f4, ok16, f4, ok16, None, 100, 128, 0, 0, ok16, ctypes.byref(t), ctypes.byref(t), ok16,
              1 << 20, None) == F.FP4_ERR_UNSUPPORTED_SHAPE
+
+
+def test_noalloc_checks_arguments_before_the_scratch_size():
+    """fp4_quantize_noalloc fails an invalid call the way fp4_quantize does,
+    even when the shape would also exceed its static scratch; undefined view
+    or flag bits are rejected by the workspace query as by the quantizer."""
+    L = F.load()
+    f = L.fp4_quantize_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_uint,
+                  ctypes.c_uint, ctypes.c_uint64, ctypes.c_uint64, ctypes.POINTER(ctypes.c_int8),
+                  ctypes.POINTER(F.fp4_tensor), ctypes.POINTER(F.fp4_tensor), ctypes.c_void_p]
+    rows, cols = 128 * 4096, 128  # needs more amax slots than the scratch holds
+    t = _t(route=F.FP4_ROUTE_NVFP4_GLOBAL, oc=1)
+    # a missing row view (requested) is an invalid argument, not a workspace error
+    assert f(16, rows, cols, cols, F.FP4_ROUTE_NVFP4_GLOBAL, 3, 0, 0, 0, None, None, ctypes.byref(t), None) == \
+        F.FP4_ERR_INVALID_ARG
+    # ld < cols, and undefined flag bits: invalid arguments too
+    assert f(16, rows, cols, cols - 8, F.FP4_ROUTE_NVFP4_GLOBAL, 3, 0, 0, 0, None, ctypes.byref(t), ctypes.byref(t),
+             None) == F.FP4_ERR_INVALID_ARG
+    assert f(16, rows, cols, cols, F.FP4_ROUTE_NVFP4_GLOBAL, 3, 0x100, 0, 0, None, ctypes.byref(t), ctypes.byref(t),
+             None) == F.FP4_ERR_INVALID_ARG
+    n = ctypes.c_size_t()
+    assert L.fp4_quantize_workspace_bytes(F.FP4_ROUTE_NVFP4_GLOBAL, 256, 256, 3, 0x100, ctypes.byref(n)) == \
+        F.FP4_ERR_INVALID_ARG
+    assert L.fp4_quantize_workspace_bytes(F.FP4_ROUTE_NVFP4_GLOBAL, 256, 256, 4, 0, ctypes.byref(n)) == \
+        F.FP4_ERR_INVALID_ARG

@@ -27,6 +27,7 @@ from fp4_quantized_linears_gb300.stack import BlockShape, FP4LinearStack
 from masked import assert_view_masked, oriented
 from masked import host_view as mhost
 from synthetic import config_tensors, normal_bf16
+from parity_stats import record
 
 pytestmark = pytest.mark.gpu
 
@@ -77,8 +78,9 @@ def check_sampled(out: torch.Tensor, a: dict, b: dict, what: str, rng):
     ref, absref = oracle.gemm_sampled(a, b, ms, ns)
     fro = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
     err = np.abs(got - ref)
-    assert fro <= REL_FRO, f"{what}: relative Frobenius {fro:.3e} over the sample"
     ratio = (err / np.maximum(absref, 1e-300)).max()
+    record(what, fro=fro, err_over_sum_abs=ratio)
+    assert fro <= REL_FRO, f"{what}: relative Frobenius {fro:.3e} over the sample"
     assert (err <= PER_ELEM * absref + 1e-30).all(), f"{what}: max err / sum|ab| = {ratio:.3e}"
 
 

@@ -16,6 +16,7 @@ import oracle
 import fp4_quantized_linears_gb300 as F
 from layout import swizzle_scales
 from synthetic import config_tensors, normal_bf16, with_outliers_bf16
+from parity_stats import record
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +41,7 @@ def assert_close(got: np.ndarray, ref: np.ndarray, absref: np.ndarray, what: str
     err = np.abs(got.astype(np.float64) - ref)
     fro = np.linalg.norm(got.astype(np.float64) - ref) / max(np.linalg.norm(ref), 1e-300)
     ratio = (err / np.maximum(absref, 1e-300)).max()
+    record(what, fro=fro, err_over_sum_abs=ratio)
     assert fro <= REL_FRO, f"{what}: relative Frobenius {fro:.3e}"
     assert (err <= PER_ELEM * absref + 1e-30).all(), f"{what}: max err / sum|ab| = {ratio:.3e} (> 2^-18)"
 

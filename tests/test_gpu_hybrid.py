@@ -14,6 +14,7 @@ import oracle
 import fp4_quantized_linears_gb300 as F
 from masked import host_view as mhost
 from synthetic import config_tensors, hadamard_signs, normal_bf16, with_outliers_bf16
+from parity_stats import record
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +42,7 @@ def close(got, a, b, what):
     ref, absref = oracle.gemm(a, b), oracle.gemm_abs(a, b)
     g = got.astype(np.float64)
     fro = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300)
+    record(what, fro=fro, err_over_sum_abs=(np.abs(g - ref) / np.maximum(absref, 1e-300)).max())
     assert fro <= REL_FRO, f"{what}: relative Frobenius {fro:.3e}"
     assert (np.abs(g - ref) <= PER_ELEM * absref + 1e-30).all(), what
 
