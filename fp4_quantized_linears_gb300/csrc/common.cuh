@@ -189,6 +189,33 @@ FP4_DEV float nv_senc(float amax) {
     return isinf(s) ? 3.402823466e38f : s;
 }
 
+// fl32(a / 6) for a block maximum that is a bf16 value (held as binary32):
+// the product with fl32(1/6), then one FMA correction with the exact
+// remainder (division by a constant known in advance, after Markstein;
+// Brisebarre, Muller and Raina, IEEE Trans. Computers 53(8), 2004).  Checked
+// equal to the correctly rounded quotient for every finite positive bf16
+// value, subnormals included; binary32 maxima of other origin take __fdiv_rn.
+FP4_DEV float div6_bf16(float a) {
+    const float c = __uint_as_float(0x3E2AAAABu);  // fl32(1/6)
+    const float q = __fmul_rn(a, c);
+    const float r = __fmaf_rn(-q, 6.0f, a);
+    return __fmaf_rn(r, c, q);
+}
+
+// The multipliers m[d] = fl32(S_enc / E4M3(d)) (0 for d = 0) of one outer
+// factor, computed once per tile into a 128-entry table (d <= 126: the
+// saturating encoder never returns the NaN code 127).
+FP4_DEV float nv_mult_entry(float senc, uint32_t d) { return d == 0 ? 0.0f : __fdiv_rn(senc, e4m3_value(d)); }
+
+// Block scale byte and multiplier of a 16-value block whose maximum is a bf16
+// value, with the multiplier read from a table of nv_mult_entry; the same
+// results as nv_block_scale.
+FP4_DEV uint32_t nv_block_scale_bf16(float block_amax, float senc, const float* mtab, float& mult) {
+    const uint32_t d = e4m3_rn_satfinite(__fmul_rn(div6_bf16(block_amax), senc));
+    mult = mtab[d];
+    return d;
+}
+
 // Block scale byte and binary32 multiplier of one 16-value block:
 // s_raw = fl32(fl32(a_b / 6) * S_enc), delta = E4M3(s_raw),
 // m_b = delta == 0 ? 0 : fl32(S_enc / delta).

@@ -48,6 +48,7 @@ struct SmemQ {
     float tile_m[64];                // 2D16: per 16x16 tile multiplier
     uint32_t tile_d[64];             // 2D16: per 16x16 tile E4M3 byte
     uint32_t seg_amax[TILE * 8];     // 2D: |max| bits of each 16-value row piece
+    float mtab[2][128];              // NVFP4: S_enc / E4M3(d) of the row / column view's factor
     uint32_t red[THREADS / 32];
 };
 
@@ -278,14 +279,21 @@ FP4_DEV void check_finite(uint32_t amax_bits) {
 // Scale choice of one 32-value segment (MX: one block; NV: two blocks of 16)
 // from the fp32 bit patterns of the blocks' amax; stages the scale bytes and
 // returns the two multipliers.
+// NVFP4: with mtab the block maxima are bf16 values and the multipliers come
+// from the tile's table; without it (H16-transformed binary32 values) both
+// quotients are divided out.
 template <bool NV>
 FP4_DEV void segment_scale(uint32_t am0, uint32_t am1, float senc, uint8_t* sc_base, int lr, int lj, float& m0,
-                           float& m1) {
+                           float& m1, const float* mtab = nullptr) {
     if (!NV) {
         check_finite(am0);
         const int e = e8m0_exponent_up(am0);
         m0 = m1 = exp2_neg(e);
         sc_base[atom_off(lr, lj)] = (uint8_t)(e + 127);
+    } else if (mtab) {
+        check_finite(max(am0, am1));
+        sc_base[atom_off(lr, 2 * lj)] = (uint8_t)nv_block_scale_bf16(__uint_as_float(am0), senc, mtab, m0);
+        sc_base[atom_off(lr, 2 * lj + 1)] = (uint8_t)nv_block_scale_bf16(__uint_as_float(am1), senc, mtab, m1);
     } else {
         check_finite(max(am0, am1));
         sc_base[atom_off(lr, 2 * lj)] = (uint8_t)nv_block_scale(__uint_as_float(am0), senc, m0);
@@ -329,6 +337,13 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             else
                 senc_col = nv_senc(__uint_as_float(ws[1 + (p.R >> 7) + tx]));
         }
+        // the multipliers S_enc / E4M3(d) of both views' factors, one
+        // division per thread (visible after the barrier below)
+        if (t < 128) {
+            if (NVR) s.mtab[0][t] = nv_mult_entry(senc_row, (uint32_t)t);
+        } else {
+            if (NVC) s.mtab[1][t - 128] = nv_mult_entry(w2d ? senc_w : senc_col, (uint32_t)(t - 128));
+        }
         if (t == 0) {
             if (NVR && do_row) {
                 if (p.row_route == FP4_ROUTE_NVFP4_LOCAL && !w2d) {
@@ -345,6 +360,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 }
             }
         }
+        __syncthreads();  // the multiplier tables
     }
 
     // 2. shared 2D weight scales: the maxima of the 16-value pieces of every
@@ -395,7 +411,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             if (part == 0) {
                 check_finite(m);
                 float mm;
-                s.tile_d[tile] = nv_block_scale(__uint_as_float(m), senc_w, mm);
+                s.tile_d[tile] = nv_block_scale_bf16(__uint_as_float(m), senc_w, s.mtab[NVR ? 0 : 1], mm);
                 s.tile_m[tile] = mm;
             }
         }
@@ -434,7 +450,8 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             } else {
                 const uint32_t a0 = amax_words<8>(w), a1 = amax_words<8>(w + 8);
                 segment_scale<true>(max(lane_lo_f32bits(a0), lane_hi_f32bits(a0)),
-                                    max(lane_lo_f32bits(a1), lane_hi_f32bits(a1)), senc_row, s.row_sc, r, j, m0, m1);
+                                    max(lane_lo_f32bits(a1), lane_hi_f32bits(a1)), senc_row, s.row_sc, r, j, m0, m1,
+                                    s.mtab[0]);
             }
             uint4 packed;
             if (sr) {
@@ -509,7 +526,8 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 else
                     segment_scale<false>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
             } else {
-                segment_scale<NVC>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1);
+                segment_scale<NVC>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1,
+                                   NVC ? s.mtab[1] : nullptr);
             }
             *reinterpret_cast<uint4*>(&s.col_codes[col_stage_off(c, j)]) = pack_rn32(v, m0, m1);
         }
@@ -679,6 +697,68 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(const __grid_constant_
     }
 }
 
+// The same maxima streamed without a pre-op or H16 (the common case): each
+// CTA of a grid sized to the resident slots walks tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... (row-strip-major), issuing the next tile's eight
+// 16-byte loads per thread before it reduces the current tile, so every
+// thread keeps a tile's loads in flight; one atomic per tile for its row strip
+// and its column strip, one per CTA for the tensor.
+__global__ void __launch_bounds__(THREADS) nv_amax_stream_kernel(const __grid_constant__ QuantParams p) {
+    __shared__ uint32_t red[THREADS / 32];
+    uint32_t* ws = p.amax_ws;
+    const int t = threadIdx.x;
+    const int64_t tiles_x = p.C / TILE, n_tiles = tiles_x * (p.R / TILE), n_row_strips = p.R / TILE;
+    uint4 d[8];
+    auto load = [&](int64_t tl) {
+        const int64_t r0 = (tl / tiles_x) * TILE, c0 = (tl % tiles_x) * TILE;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = t + i * THREADS;
+            d[i] = *reinterpret_cast<const uint4*>(p.x + (r0 + (q >> 4)) * p.ld + c0 + (q & 15) * 8);
+        }
+    };
+    uint32_t mt = 0;  // this CTA's running tensor maximum (fp32 bits)
+    int64_t tile = blockIdx.x;
+    if (tile < n_tiles) load(tile);
+    for (; tile < n_tiles; tile += gridDim.x) {
+        uint32_t m2 = 0;  // per 16-bit lane maxima of |bf16|
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            m2 = __vimax3_u16x2(m2, d[i].x & 0x7FFF7FFFu, d[i].y & 0x7FFF7FFFu);
+            m2 = __vimax3_u16x2(m2, d[i].z & 0x7FFF7FFFu, d[i].w & 0x7FFF7FFFu);
+        }
+        if (tile + gridDim.x < n_tiles) load(tile + gridDim.x);
+        uint32_t m = max(m2 << 16, m2 & 0xFFFF0000u);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if ((t & 31) == 0) red[t >> 5] = m;
+        __syncthreads();
+        if (t == 0) {
+            for (int i = 1; i < THREADS / 32; ++i) m = max(m, red[i]);
+            atomicMax(&ws[1 + tile / tiles_x], m);
+            atomicMax(&ws[1 + n_row_strips + tile % tiles_x], m);
+            mt = max(mt, m);
+        }
+        __syncthreads();  // red is reused by the next tile
+    }
+    if (t == 0 && mt) {
+        check_finite(mt);
+        atomicMax(&ws[0], mt);
+    }
+}
+
+int quant_sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
 // CTAs of the encoder: two tiles per CTA, so that the second tile's load
 // overlaps the first one's encoding.  (Measured against one tile per CTA and
 // against one CTA per resident slot looping over all tiles: two per CTA was
@@ -729,9 +809,15 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
     if (slots) {
         if (cudaMemsetAsync(p.amax_ws, 0, slots * 4, stream) != cudaSuccess) return FP4_ERR_CUDA;
         const bool col_h16 = (p.flags & FP4_FLAG_HADAMARD16_COL) && do_col && p.col_route != FP4_ROUTE_MXFP4;
-        const size_t amax_smem = (p.pre != PRE_NONE || col_h16) ? sizeof(uint16_t) * TILE * LDS : 0;
-        dim3 grid((unsigned)(p.C / TILE), (unsigned)(p.R / TILE));
-        nv_amax_kernel<<<grid, THREADS, amax_smem, stream>>>(p);
+        if (p.pre != PRE_NONE || col_h16) {
+            const size_t amax_smem = sizeof(uint16_t) * TILE * LDS;
+            dim3 grid((unsigned)(p.C / TILE), (unsigned)(p.R / TILE));
+            nv_amax_kernel<<<grid, THREADS, amax_smem, stream>>>(p);
+        } else {
+            const int64_t n_tiles = (p.C / TILE) * (p.R / TILE);
+            const int64_t slots = (int64_t)quant_sm_count() * 4;  // 256 threads x 64 registers: four CTAs per SM
+            nv_amax_stream_kernel<<<(unsigned)(n_tiles < slots ? n_tiles : slots), THREADS, 0, stream>>>(p);
+        }
         if (cudaGetLastError() != cudaSuccess) return FP4_ERR_CUDA;
     }
     if (nvr && nvc) return launch_encoder<true, true>(p, stream);
