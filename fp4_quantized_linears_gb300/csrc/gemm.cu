@@ -319,6 +319,29 @@ FP4_DEV void tmem_ld32(uint32_t taddr, uint32_t* r) {
         : "r"(taddr)
         : "memory");
 }
+// Two 32-column loads (at ta and tb) under one wait.
+FP4_DEV void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t* a, uint32_t* b) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31"
+        "}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
+        "}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+          "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+          "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
+          "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
+          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+          "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]),
+          "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]),
+          "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
 // Two 64-column loads (at ta and tb) under one wait.
 FP4_DEV void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t* a, uint32_t* b) {
     asm volatile(
@@ -447,6 +470,29 @@ FP4_DEV uint32_t mx_words_sr(const uint32_t* w, uint64_t g0, const uint32_t* rk,
     return (uint32_t)(e + 127);
 }
 
+// MX block of the 32 bf16 values of 16 words, round to nearest: scale byte
+// and 16 bytes of codes.
+FP4_DEV uint32_t mx_words_rn(const uint32_t* w, uint4& packed) {
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
+    const uint32_t am = lanes_max_f32bits(m2);
+    if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
+    const int e = e8m0_exponent_up(am);
+    const float mult = exp2_neg(e);
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float s8[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            f32x2_mul(s8[2 * b], s8[2 * b + 1], bf16_lo(w[4 * q + b]), bf16_hi(w[4 * q + b]), mult, mult);
+        out[q] = e2m1x8_rn(s8[0], s8[1], s8[2], s8[3], s8[4], s8[5], s8[6], s8[7]);
+    }
+    packed = make_uint4(out[0], out[1], out[2], out[3]);
+    return (uint32_t)(e + 127);
+}
+
 // MX block of the low (h = 0) or high (h = 1) bf16 lanes of 32 words, round
 // to nearest; am = fp32 bits of the block's maximum magnitude.
 FP4_DEV uint32_t mx_lane_rn(const uint32_t* w, int h, uint32_t am, uint4& packed) {
@@ -498,11 +544,13 @@ FP4_DEV void store_bf16x32(uint16_t* dst, const float* v) {
 // store's register allocation is untouched)
 enum { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_QKV_ROPE = 3, EPI_STORE_RMS = 4 };
 __host__ __device__ constexpr bool is_store(int epi) { return epi == EPI_STORE || epi == EPI_STORE_RMS; }
-// The SwiGLU backward's epilogue (SiLU derivative, two SR row views, two
-// transposed column views per tile) is latency-bound: it runs on 16 warps,
+// The SwiGLU epilogues (the gate or its derivative, the row views, the
+// transposed column views per tile) are latency-bound: they run on 16 warps,
 // each thread holding one row x 32 columns; the others on 8 (one row x 64 or
 // 128 columns).
-__host__ __device__ constexpr int epi_warps(int epi) { return epi == EPI_SWIGLU_BWD ? 16 : EPI_WARPS; }
+__host__ __device__ constexpr int epi_warps(int epi) {
+    return epi == EPI_SWIGLU_BWD || epi == EPI_SWIGLU_FWD ? 16 : EPI_WARPS;
+}
 __host__ __device__ constexpr int kthreads(int epi) { return 32 * (2 + epi_warps(epi) + SF_WARPS); }
 
 struct KParams {
@@ -937,9 +985,13 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
             epi_phase ^= 1;
         };
         // SwiGLU backward (pairs): this thread's a1 / a3 row segments of a
-        // tile are copied into its own shared slot one tile ahead, so that
-        // their latency hides behind the previous tile's work
-        const uint32_t slot = smem_u32(staging + 2 * BM * ST_LDS * 2 + 4 * 512) + (uint32_t)et * 128;
+        // tile are copied into shared memory one tile ahead, so that their
+        // latency hides behind the previous tile's work.  Chunk-major layout:
+        // 16-byte chunk i (a1: 0-3, a3: 4-7) of epilogue thread et sits at
+        // (i * 32 * EW + et) * 16, so a warp's accesses to one chunk are 512
+        // contiguous bytes (no bank conflicts).
+        const uint32_t slot = smem_u32(staging + 2 * BM * ST_LDS * 2 + 4 * 512) + (uint32_t)et * 16;
+        constexpr uint32_t CHUNK_STRIDE = 32 * EW * 16;
         auto prefetch_a13 = [&](int64_t u2) {
             if constexpr (C::BWD_PREFETCH) {
                 if (u2 < n_units) {
@@ -948,8 +1000,8 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     const int64_t off = (m2 + lr) * p.f + n2 + 32 * half;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        cp_async16(slot + 16 * i, p.a1 + off + 8 * i);
-                        cp_async16(slot + 64 + 16 * i, p.a3 + off + 8 * i);
+                        cp_async16(slot + i * CHUNK_STRIDE, p.a1 + off + 8 * i);
+                        cp_async16(slot + (4 + i) * CHUNK_STRIDE, p.a3 + off + 8 * i);
                     }
                 }
                 cp_async_commit();
@@ -1163,12 +1215,14 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                         *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
                 }
             } else if constexpr (EPI == EPI_SWIGLU_FWD) {
-                // output columns [64*half, 64*half + 64) of this 128-wide tile:
-                // a1 in accumulator columns 0..127, a3 in 128..255
-                uint32_t p1[32], p3[32];  // bf16x2 of the retained a1, a3 (64 columns each)
+                // output columns [oc, oc + 32) of this 128-wide tile: a1 in
+                // accumulator columns oc .., a3 in 128 + oc ..
+                const int oc = 32 * half;
+                const int64_t n = n0 + oc;
+                uint32_t p1[16], p3[16];  // bf16x2 of the retained a1, a3
                 {
-                    uint32_t r1[64], r3[64];
-                    tmem_ld64x2(lane_base + 64 * half, lane_base + 128 + 64 * half, r1, r3);
+                    uint32_t r1[32], r3[32];
+                    tmem_ld32x2(lane_base + oc, lane_base + 128 + oc, r1, r3);
                     tc_fence_before();
                     release_acc();
                     float alpha = 1.0f;
@@ -1176,7 +1230,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                         alpha = __fmul_rn(__fdiv_rn(1.0f, p.a_outer[p.a_outer_count == 1 ? 0 : (m0 >> 7)]),
                                           __fdiv_rn(1.0f, p.b_outer[0]));
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         p1[i] = bf16x2_rn(__uint_as_float(r1[2 * i]) * alpha, __uint_as_float(r1[2 * i + 1]) * alpha);
                         p3[i] = bf16x2_rn(__uint_as_float(r3[2 * i]) * alpha, __uint_as_float(r3[2 * i + 1]) * alpha);
                     }
@@ -1184,61 +1238,48 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 uint16_t* hs = reinterpret_cast<uint16_t*>(staging);
                 uint8_t* row_atom = staging + BM * ST_LDS * 2;
                 uint8_t* col_atom = row_atom + 512;
+                store_words16(p.a1 + m * p.f + n, p1);
+                store_words16(p.a3 + m * p.f + n, p3);
+                uint32_t hp[16];  // bf16x2 of h = bf16(fl32(SiLU(a1)) * a3)
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int oc = 64 * half + 32 * c;
-                    const int64_t n = n0 + oc;
-                    store_words16(p.a1 + m * p.f + n, p1 + 16 * c);
-                    store_words16(p.a3 + m * p.f + n, p3 + 16 * c);
-                    float h[32];
-                    uint32_t hp[16];
+                for (int i = 0; i < 16; ++i) {
+                    float hv[2];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint32_t w1 = p1[16 * c + i], w3 = p3[16 * c + i];
-                        float hv[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const float x1 = e ? bf16_hi(w1) : bf16_lo(w1);
-                            const float x3 = e ? bf16_hi(w3) : bf16_lo(w3);
-                            const float sl = x1 * __fdividef(1.0f, 1.0f + __expf(-x1));
-                            hv[e] = __fmul_rn(sl, x3);
-                        }
-                        hp[i] = bf16x2_rn(hv[0], hv[1]);
-                        h[2 * i] = bf16_lo(hp[i]);
-                        h[2 * i + 1] = bf16_hi(hp[i]);
+                    for (int e = 0; e < 2; ++e) {
+                        const float x1 = e ? bf16_hi(p1[i]) : bf16_lo(p1[i]);
+                        const float x3 = e ? bf16_hi(p3[i]) : bf16_lo(p3[i]);
+                        const float sl = x1 * __fdividef(1.0f, 1.0f + __expf(-x1));
+                        hv[e] = __fmul_rn(sl, x3);
                     }
-                    if (p.tap0) store_words16(p.tap0 + m * p.f + n, hp);
-                    if (p.quantize) {
-                        uint4 pk;
-                        uint32_t sc = mx_block_rn(h, pk);
-                        *reinterpret_cast<uint4*>(p.q_row_codes + m * (p.f >> 1) + (n >> 1)) = pk;
-                        row_atom[atom_off(lr, oc >> 5)] = (uint8_t)sc;
-                        store_words16(hs + lr * ST_LDS + oc, hp);
-                    }
+                    hp[i] = bf16x2_rn(hv[0], hv[1]);
                 }
+                if (p.tap0) store_words16(p.tap0 + m * p.f + n, hp);
                 if (p.quantize) {
+                    uint4 pk;
+                    const uint32_t sc = mx_words_rn(hp, pk);
+                    *reinterpret_cast<uint4*>(p.q_row_codes + m * (p.f >> 1) + (n >> 1)) = pk;
+                    row_atom[atom_off(lr, half)] = (uint8_t)sc;
+                    store_words16(hs + lr * ST_LDS + oc, hp);
                     epi_sync();
                     if (!epi_ok) break;
-                    // column-facing view: stored row = output column, blocks along the tokens
-                    // column pairs: one 32-bit load per two values
+                    // column-facing view: stored row = output column, blocks
+                    // along the tokens; thread = (32-row block j, column c),
+                    // reading the column-pair words down the block (two
+                    // neighbouring threads share each word)
                     {
-                        const int j = et >> 6, cp = et & 63;
+                        const int c = et & 127, j = et >> 7;
                         uint32_t w[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            w[i] = *reinterpret_cast<const uint32_t*>(&hs[(32 * j + i) * ST_LDS + 2 * cp]);
+                            w[i] = *reinterpret_cast<const uint32_t*>(&hs[(32 * j + i) * ST_LDS + (c & ~1)]);
+                        uint32_t m2 = 0;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int cidx = 2 * cp + h;
-                            float v[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
-                            uint4 pk;
-                            uint32_t sc = mx_block_rn(v, pk);
-                            *reinterpret_cast<uint4*>(p.q_col_codes + (n0 + cidx) * (p.M >> 1) +
-                                                      ((m0 + 32 * j) >> 1)) = pk;
-                            col_atom[atom_off(cidx, j)] = (uint8_t)sc;
-                        }
+                        for (int i = 0; i < 32; i += 2)
+                            m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
+                        uint4 pkc;
+                        const uint32_t scc = mx_lane_rn(w, c & 1, (c & 1) ? (m2 & 0xFFFF0000u) : (m2 << 16), pkc);
+                        *reinterpret_cast<uint4*>(p.q_col_codes + (n0 + c) * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pkc;
+                        col_atom[atom_off(c, j)] = (uint8_t)scc;
                     }
                     epi_sync();
                     if (!epi_ok) break;
@@ -1283,12 +1324,11 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     uint4 v1[4], v3[4];
                     if constexpr (C::BWD_PREFETCH) {
                         cp_async_wait_all();  // this thread's own copies of this tile's segments
-                        const uint4* s13 = reinterpret_cast<const uint4*>(staging + 2 * BM * ST_LDS * 2 + 4 * 512 +
-                                                                          et * 128);
+                        const uint8_t* s13 = staging + 2 * BM * ST_LDS * 2 + 4 * 512 + et * 16;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            v1[i] = s13[i];
-                            v3[i] = s13[4 + i];
+                            v1[i] = *reinterpret_cast<const uint4*>(s13 + i * CHUNK_STRIDE);
+                            v3[i] = *reinterpret_cast<const uint4*>(s13 + (4 + i) * CHUNK_STRIDE);
                         }
                     } else {
                         const uint4* pa1 = reinterpret_cast<const uint4*>(p.a1 + m * p.f + n);
