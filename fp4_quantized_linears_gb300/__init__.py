@@ -116,8 +116,10 @@ def _declare(L):
                                                           vp, vp, c_i64, c_i64, c_u64, c_u64, vp, tp, tp, vp, c_sz,
                                                           vp]),
         "fp4_rmsnorm_bwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int, c_i64, c_i64, ctypes.POINTER(c_sz)]),
-        "fp4_swiglu_fwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, tp, tp, vp, vp]),
-        "fp4_swiglu_bwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, c_u64, c_u64, tp, tp, vp, vp, vp]),
+        "fp4_swiglu_fwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, tp, tp, vp, vp, c_sz, vp]),
+        "fp4_swiglu_bwd": (ctypes.c_int, [tp, tp, c_i64, vp, vp, c_u64, c_u64, tp, tp, vp, vp, vp, c_sz, vp]),
+        "fp4_swiglu_workspace_bytes": (ctypes.c_int, [ctypes.c_int, c_i64, c_i64, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.POINTER(c_sz)]),
         "fp4_qkv_rope_fwd": (ctypes.c_int, [tp, tp, vp, vp, c_i64, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]),
         "fp4_qkv_rope_bwd": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint, ctypes.c_int, vp, vp, vp, vp, vp, c_i64, c_i64,
                                             ctypes.c_int, ctypes.c_int, c_u64, c_u64, vp, tp, tp, vp, c_sz, vp]),
@@ -413,20 +415,37 @@ def fp4_residual_rmsnorm_bwd_parts(dy: torch.Tensor, part: torch.Tensor, r_prime
     return dr, dr_row, dr_col
 
 
+def fp4_swiglu_workspace_bytes(route, T: int, f: int, backward: bool = False, with_tap: bool = False) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fp4_swiglu_workspace_bytes(_route(route), T, f, 1 if backward else 0, 1 if with_tap else 0,
+                                             ctypes.byref(n)), "fp4_swiglu_workspace_bytes")
+    return n.value
+
+
+def _ws_args(workspace):
+    if workspace is None:
+        return None, 0
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
 def fp4_swiglu_fwd(x_row: QView, w13_row: QView, f: int, a1=None, a3=None, h_row=None, h_col=None, h_tap=None,
-                   quantize: bool = True, stream=None):
+                   quantize: bool = True, workspace=None, stream=None):
     """Fused W1/W3 contraction + SiLU gate.  Returns (a1, a3, h_row, h_col).
 
-    For MXFP4 the FP4 views of h are emitted (unless quantize=False, then
-    h_tap must be given); for NVFP4 h_tap is required and views are None."""
+    With quantize (the default) the FP4 views of h are emitted for every
+    route (NVFP4 through one bf16 copy of h; a workspace is allocated here
+    when none is given); with quantize=False only h_tap is written."""
     T = x_row.rows
     dev = x_row.codes.device
     a1 = torch.empty((T, f), dtype=torch.bfloat16, device=dev) if a1 is None else a1
     a3 = torch.empty((T, f), dtype=torch.bfloat16, device=dev) if a3 is None else a3
-    mx = x_row.route == FP4_ROUTE_MXFP4
-    if mx and quantize:
-        h_row = alloc_view(FP4_ROUTE_MXFP4, T, f, 0, dev) if h_row is None else h_row
-        h_col = alloc_view(FP4_ROUTE_MXFP4, f, T, 0, dev) if h_col is None else h_col
+    route = x_row.route
+    if quantize:
+        h_row = alloc_view(route, T, f, 0, dev) if h_row is None else h_row
+        h_col = alloc_view(route, f, T, 0, dev) if h_col is None else h_col
+        need = fp4_swiglu_workspace_bytes(route, T, f, False, h_tap is not None)
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     else:
         h_row = h_col = None
     a, b = x_row.struct(), w13_row.struct()
@@ -434,7 +453,7 @@ def fp4_swiglu_fwd(x_row: QView, w13_row: QView, f: int, a1=None, a3=None, h_row
     cs = h_col.struct() if h_col is not None else None
     _check(load().fp4_swiglu_fwd(ctypes.byref(a), ctypes.byref(b), f, _ptr(a1), _ptr(a3),
                                  ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None, _ptr(h_tap),
-                                 _stream(stream)), "fp4_swiglu_fwd")
+                                 *_ws_args(workspace), _stream(stream)), "fp4_swiglu_fwd")
     if rs:
         _sync_fields(h_row, rs)
         _sync_fields(h_col, cs)
@@ -443,14 +462,17 @@ def fp4_swiglu_fwd(x_row: QView, w13_row: QView, f: int, a1=None, a3=None, h_row
 
 def fp4_swiglu_bwd(dy2_row: QView, w2_col: QView, f: int, a1: torch.Tensor, a3: torch.Tensor, sr_seed: int = 0,
                    sr_offset: int = 0, da13_row=None, da13_col=None, dh_tap=None, da13_tap=None,
-                   quantize: bool = True, stream=None):
+                   quantize: bool = True, workspace=None, stream=None):
     """Fused W2 Dgrad + SiLU derivative.  Returns (da13_row, da13_col)."""
     T = dy2_row.rows
     dev = dy2_row.codes.device
-    mx = dy2_row.route == FP4_ROUTE_MXFP4
-    if mx and quantize:
-        da13_row = alloc_view(FP4_ROUTE_MXFP4, T, 2 * f, 0, dev) if da13_row is None else da13_row
-        da13_col = alloc_view(FP4_ROUTE_MXFP4, 2 * f, T, 0, dev) if da13_col is None else da13_col
+    route = dy2_row.route
+    if quantize:
+        da13_row = alloc_view(route, T, 2 * f, FP4_FLAG_SR_ROW, dev) if da13_row is None else da13_row
+        da13_col = alloc_view(route, 2 * f, T, 0, dev) if da13_col is None else da13_col
+        need = fp4_swiglu_workspace_bytes(route, T, f, True, da13_tap is not None)
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     else:
         da13_row = da13_col = None
     a, b = dy2_row.struct(), w2_col.struct()
@@ -458,7 +480,7 @@ def fp4_swiglu_bwd(dy2_row: QView, w2_col: QView, f: int, a1: torch.Tensor, a3: 
     cs = da13_col.struct() if da13_col is not None else None
     _check(load().fp4_swiglu_bwd(ctypes.byref(a), ctypes.byref(b), f, _ptr(a1), _ptr(a3), sr_seed, sr_offset,
                                  ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None, _ptr(dh_tap),
-                                 _ptr(da13_tap), _stream(stream)), "fp4_swiglu_bwd")
+                                 _ptr(da13_tap), *_ws_args(workspace), _stream(stream)), "fp4_swiglu_bwd")
     if rs:
         _sync_fields(da13_row, rs)
         _sync_fields(da13_col, cs)

@@ -182,8 +182,19 @@ int fp4_residual_rmsnorm_fwd(int route, unsigned views, const void* r, const voi
         return FP4_ERR_INVALID_ARG;
     if (!(eps >= 0.0f)) return FP4_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_rmsnorm_fwd_stats(static_cast<const uint16_t*>(r), static_cast<const uint16_t*>(b), rows, cols, ld,
-                                  eps, static_cast<uint16_t*>(r_out), rstd, s);
+    const size_t slots = quant_workspace_slots(rows, cols, route, route, views, 0);
+    if (slots) {
+        // NVFP4: the row pass also folds the maxima of y, so the encoder
+        // needs no pass of its own over the rows before it
+        if (cudaMemsetAsync(p.amax_ws, 0, slots * 4, s) != cudaSuccess) return FP4_ERR_CUDA;
+        rc = launch_rmsnorm_fwd_stats_amax(static_cast<const uint16_t*>(r), static_cast<const uint16_t*>(b),
+                                           static_cast<const uint16_t*>(g), rows, cols, ld, eps,
+                                           static_cast<uint16_t*>(r_out), rstd, p.amax_ws, s);
+        p.amax_ready = 1;
+    } else {
+        rc = launch_rmsnorm_fwd_stats(static_cast<const uint16_t*>(r), static_cast<const uint16_t*>(b), rows, cols,
+                                      ld, eps, static_cast<uint16_t*>(r_out), rstd, s);
+    }
     if (rc != FP4_OK) return rc;
     p.pre = PRE_RMSNORM_FWD;
     p.rstd = rstd;
@@ -396,8 +407,37 @@ int fp4_qkv_rope_bwd(int route, unsigned views, int sr, const void* dq, const vo
     return launch_quantize(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Workspace of the NVFP4 gated-FFN producers: the amax slots of the tensor
+// that is encoded (h [T][f] forward, [da1 | da3] [T][2f] backward), padded to
+// 256 bytes, then its bf16 copy unless the caller passes a tap for it.
+static size_t swiglu_slots_bytes(int64_t T, int64_t cols) {
+    return ((size_t)(1 + T / 128 + cols / 128) * 4 + 255) / 256 * 256;
+}
+
+int fp4_swiglu_workspace_bytes(int route, int64_t T, int64_t f, int backward, int with_tap, size_t* bytes) {
+    if (!route_ok(route) || !bytes || T < 0 || f < 0) return FP4_ERR_INVALID_ARG;
+    if (T % 128 || f % 128) return FP4_ERR_UNSUPPORTED_SHAPE;
+    const int64_t cols = backward ? 2 * f : f;
+    *bytes = route == FP4_ROUTE_MXFP4 ? 0 : swiglu_slots_bytes(T, cols) + (with_tap ? 0 : (size_t)(T * cols * 2));
+    return FP4_OK;
+}
+
+// The NVFP4 encode of a gated-FFN tap: the epilogue has already written the
+// tap and folded its maxima into the slots (zeroed before the contraction).
+static int encode_tap(const uint16_t* tap, int64_t T, int64_t cols, int route, unsigned flags, uint64_t seed,
+                      uint64_t offset, fp4_tensor* row, fp4_tensor* col, void* slots, size_t slots_bytes,
+                      cudaStream_t s) {
+    QuantParams q;
+    int rc = prepare_quant(tap, false, T, cols, cols, route, route, 3, flags, seed, offset, nullptr, row, col, slots,
+                           slots_bytes, &q);
+    if (rc != FP4_OK) return rc;
+    q.amax_ready = 1;
+    return launch_quantize(q, s);
+}
+
 int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f, void* a1, void* a3,
-                   fp4_tensor* h_row, fp4_tensor* h_col, void* h_tap, fp4_stream_t stream) {
+                   fp4_tensor* h_row, fp4_tensor* h_col, void* h_tap, void* workspace, size_t workspace_bytes,
+                   fp4_stream_t stream) {
     int rc;
     if ((rc = check_operand(x_row)) != FP4_OK || (rc = check_operand(w13_row)) != FP4_OK) return rc;
     if (x_row->route != w13_row->route) return FP4_ERR_ROUTE_MISMATCH;
@@ -407,13 +447,15 @@ int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f
     if (!a1 || !a3 || !aligned16(a1) || !aligned16(a3) || (h_tap && !aligned16(h_tap))) return FP4_ERR_INVALID_ARG;
     const bool mx = x_row->route == FP4_ROUTE_MXFP4;
     if (w13_row->route != FP4_ROUTE_MXFP4 && w13_row->outer_count != 1) return FP4_ERR_INVALID_ARG;
-    if (mx) {
-        if ((h_row == nullptr) != (h_col == nullptr)) return FP4_ERR_INVALID_ARG;
-        if (h_row && (!view_ok(h_row) || !view_ok(h_col))) return FP4_ERR_INVALID_ARG;
-        if (!h_row && !h_tap) return FP4_ERR_INVALID_ARG;
-    } else {
-        if (h_row || h_col) return FP4_ERR_ROUTE_MISMATCH;
-        if (!h_tap) return FP4_ERR_INVALID_ARG;
+    if ((h_row == nullptr) != (h_col == nullptr)) return FP4_ERR_INVALID_ARG;
+    if (h_row && (!view_ok(h_row) || !view_ok(h_col))) return FP4_ERR_INVALID_ARG;
+    if (!h_row && !h_tap) return FP4_ERR_INVALID_ARG;
+    const bool nv_views = !mx && h_row;
+    size_t need = 0;
+    if (nv_views) {
+        if ((rc = fp4_swiglu_workspace_bytes(x_row->route, T, f, 0, h_tap != nullptr, &need)) != FP4_OK) return rc;
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FP4_ERR_WORKSPACE;
+        if (!h_row->outer || !h_col->outer) return FP4_ERR_INVALID_ARG;
     }
     GemmParams g{};
     fill_operands(g, x_row, w13_row);
@@ -425,6 +467,7 @@ int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f
     g.a1 = static_cast<uint16_t*>(a1);
     g.a3 = static_cast<uint16_t*>(a3);
     g.tap0 = static_cast<uint16_t*>(h_tap);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (mx && h_row) {
         g.quantize = 1;
         g.q_row_codes = static_cast<uint8_t*>(h_row->codes);
@@ -433,13 +476,25 @@ int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f
         g.q_col_scales = static_cast<uint8_t*>(h_col->scales);
         set_view(h_row, T, f, FP4_ROUTE_MXFP4);
         set_view(h_col, f, T, FP4_ROUTE_MXFP4);
+        return launch_gemm(g, s);
     }
-    return launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
+    if (!nv_views) return launch_gemm(g, s);
+    // NVFP4: every strip factor depends on values from the whole strip (all f
+    // columns for the row view, all T tokens for the column view), so h goes
+    // through one bf16 copy: the epilogue writes it and folds its maxima, the
+    // encoder reads it once
+    const size_t sb = swiglu_slots_bytes(T, f);
+    uint32_t* slots = static_cast<uint32_t*>(workspace);
+    g.tap0 = h_tap ? static_cast<uint16_t*>(h_tap) : reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + sb);
+    g.amax_ws = slots;
+    if (cudaMemsetAsync(slots, 0, sb, s) != cudaSuccess) return FP4_ERR_CUDA;
+    if ((rc = launch_gemm(g, s)) != FP4_OK) return rc;
+    return encode_tap(g.tap0, T, f, x_row->route, 0, 0, 0, h_row, h_col, slots, sb, s);
 }
 
 int fp4_swiglu_bwd(const fp4_tensor* dy2_row, const fp4_tensor* w2_col, int64_t f, const void* a1, const void* a3,
                    uint64_t sr_seed, uint64_t sr_offset, fp4_tensor* da13_row, fp4_tensor* da13_col, void* dh_tap,
-                   void* da13_tap, fp4_stream_t stream) {
+                   void* da13_tap, void* workspace, size_t workspace_bytes, fp4_stream_t stream) {
     int rc;
     if ((rc = check_operand(dy2_row)) != FP4_OK || (rc = check_operand(w2_col)) != FP4_OK) return rc;
     if (dy2_row->route != w2_col->route) return FP4_ERR_ROUTE_MISMATCH;
@@ -450,13 +505,16 @@ int fp4_swiglu_bwd(const fp4_tensor* dy2_row, const fp4_tensor* w2_col, int64_t 
         (da13_tap && !aligned16(da13_tap)))
         return FP4_ERR_INVALID_ARG;
     const bool mx = dy2_row->route == FP4_ROUTE_MXFP4;
-    if (mx) {
-        if ((da13_row == nullptr) != (da13_col == nullptr)) return FP4_ERR_INVALID_ARG;
-        if (da13_row && (!view_ok(da13_row) || !view_ok(da13_col))) return FP4_ERR_INVALID_ARG;
-        if (!da13_row && !da13_tap) return FP4_ERR_INVALID_ARG;
-    } else {
-        if (da13_row || da13_col) return FP4_ERR_ROUTE_MISMATCH;
-        if (!da13_tap) return FP4_ERR_INVALID_ARG;
+    if ((da13_row == nullptr) != (da13_col == nullptr)) return FP4_ERR_INVALID_ARG;
+    if (da13_row && (!view_ok(da13_row) || !view_ok(da13_col))) return FP4_ERR_INVALID_ARG;
+    if (!da13_row && !da13_tap) return FP4_ERR_INVALID_ARG;
+    const bool nv_views = !mx && da13_row;
+    size_t need = 0;
+    if (nv_views) {
+        if ((rc = fp4_swiglu_workspace_bytes(dy2_row->route, T, f, 1, da13_tap != nullptr, &need)) != FP4_OK)
+            return rc;
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FP4_ERR_WORKSPACE;
+        if (!da13_row->outer || !da13_col->outer) return FP4_ERR_INVALID_ARG;
     }
     GemmParams g{};
     fill_operands(g, dy2_row, w2_col);
@@ -471,6 +529,7 @@ int fp4_swiglu_bwd(const fp4_tensor* dy2_row, const fp4_tensor* w2_col, int64_t 
     g.tap1 = static_cast<uint16_t*>(da13_tap);
     g.seed = sr_seed;
     g.offset = sr_offset;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (mx && da13_row) {
         g.quantize = 1;
         g.q_row_codes = static_cast<uint8_t*>(da13_row->codes);
@@ -479,8 +538,19 @@ int fp4_swiglu_bwd(const fp4_tensor* dy2_row, const fp4_tensor* w2_col, int64_t 
         g.q_col_scales = static_cast<uint8_t*>(da13_col->scales);
         set_view(da13_row, T, 2 * f, FP4_ROUTE_MXFP4);
         set_view(da13_col, 2 * f, T, FP4_ROUTE_MXFP4);
+        return launch_gemm(g, s);
     }
-    return launch_gemm(g, reinterpret_cast<cudaStream_t>(stream));
+    if (!nv_views) return launch_gemm(g, s);
+    // NVFP4: [da1 | da3] through one bf16 copy, its maxima from the epilogue
+    const size_t sb = swiglu_slots_bytes(T, 2 * f);
+    uint32_t* slots = static_cast<uint32_t*>(workspace);
+    g.tap1 = da13_tap ? static_cast<uint16_t*>(da13_tap)
+                      : reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + sb);
+    g.amax_ws = slots;
+    if (cudaMemsetAsync(slots, 0, sb, s) != cudaSuccess) return FP4_ERR_CUDA;
+    if ((rc = launch_gemm(g, s)) != FP4_OK) return rc;
+    return encode_tap(g.tap1, T, 2 * f, dy2_row->route, FP4_FLAG_SR_ROW, sr_seed, sr_offset, da13_row, da13_col,
+                      slots, sb, s);
 }
 
 int fp4_linear_fprop(const fp4_tensor* x_row, const fp4_tensor* w_row, void* y, int out_dtype, float beta,

@@ -441,6 +441,18 @@ FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
     return (uint32_t)(e + 127);
 }
 
+// Largest |bf16| of n words, as fp32 bits, reduced over the warp.
+template <int N>
+FP4_DEV uint32_t warp_amax_words(const uint32_t* w) {
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < N; i += 2) m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
+    uint32_t m = max(m2 << 16, m2 & 0xFFFF0000u);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    return m;
+}
+
 // fp32 bit pattern of the larger magnitude in a word of two bf16 maxima
 FP4_DEV uint32_t lanes_max_f32bits(uint32_t m2) { return max(m2 << 16, m2 & 0xFFFF0000u); }
 
@@ -596,6 +608,7 @@ struct KParams {
     // (n_inner = 1: N fastest, the band's B tiles reused while A streams)
     int n_inner;
     int64_t band;
+    uint32_t* amax_ws;  // SwiGLU taps for an NVFP4 encode: maxima slots, or NULL
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -634,10 +647,14 @@ struct Cfg {
     // row segments (2 x 64 bytes) of the next tile land in a slot of its own
     static constexpr bool BWD_PREFETCH = EPI == EPI_SWIGLU_BWD && P2;
     static constexpr int PREFETCH_BYTES = BWD_PREFETCH ? epi_warps(EPI) * 32 * 128 : 0;
+    // SwiGLU forward: one 2 KB box (32 rows x 64 bytes) per epilogue warp,
+    // and the row and column scale atoms of two tiles
+    static constexpr int FWD_BOX = 32 * 64;
     static constexpr int STAGING =
-        is_store(EPI)         ? EPI_WARPS * OUT_BUFS * OUT_BOX
-        : EPI == EPI_QKV_ROPE ? 0
-                              : (EPI == EPI_SWIGLU_FWD ? 1 : 2) * BM * ST_LDS * 2 + 4 * 512 + PREFETCH_BYTES;
+        is_store(EPI)          ? EPI_WARPS * OUT_BUFS * OUT_BOX
+        : EPI == EPI_QKV_ROPE  ? 0
+        : EPI == EPI_SWIGLU_FWD ? epi_warps(EPI) * FWD_BOX + 4 * 512
+                               : 2 * BM * ST_LDS * 2 + 4 * 512 + PREFETCH_BYTES;
     static constexpr int STAGES = fit(STAGING);
     static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + RESERVED;
     static_assert(STAGES >= 3, "pipeline depth");
@@ -650,7 +667,8 @@ template <bool NV, int BN, int EPI, int CM, bool P2 = false>
 __global__ void __launch_bounds__(kthreads(EPI), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
-                    const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ KParams p) {
+                    const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ KParams p) {
     using C = Cfg<NV, BN, EPI, P2>;
     static_assert(P2 ? CM == 2 : CM == 1, "clusters are CTA pairs");
     static_assert(!P2 || BN == 256 || EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD, "pair tile widths");
@@ -958,6 +976,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         uint32_t acc_phase = 0, epi_phase = 0;
         bool epi_ok = true;
         bool skip_release = p.skip_first_release != 0;  // test hook, first tile only
+        uint32_t tensor_amax = 0;  // SwiGLU taps: this warp's running maximum (fp32 bits)
         // the accumulator is free once every epilogue warp has read it; in
         // pair mode the MMA thread waits on the leader's barrier for the
         // warps of both CTAs
@@ -1215,8 +1234,14 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                         *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
                 }
             } else if constexpr (EPI == EPI_SWIGLU_FWD) {
-                // output columns [oc, oc + 32) of this 128-wide tile: a1 in
-                // accumulator columns oc .., a3 in 128 + oc ..
+                // This thread: row lr, output columns [oc, oc + 32) of the
+                // 128-wide tile (a1 in accumulator columns oc .., a3 in
+                // 128 + oc ..); this warp: the 32 x 32 block of rows
+                // [32q, 32q + 32).  The block's retained a1 and a3 leave
+                // through the warp's own 2 KB box (64-byte rows, 64B swizzle)
+                // by TMA tensor stores; the box then holds the block's h, read
+                // down its columns for the column view (the block is exactly
+                // one 32-row block of 32 stored rows of Q_c(h)).
                 const int oc = 32 * half;
                 const int64_t n = n0 + oc;
                 uint32_t p1[16], p3[16];  // bf16x2 of the retained a1, a3
@@ -1235,11 +1260,30 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                         p3[i] = bf16x2_rn(__uint_as_float(r3[2 * i]) * alpha, __uint_as_float(r3[2 * i + 1]) * alpha);
                     }
                 }
-                uint16_t* hs = reinterpret_cast<uint16_t*>(staging);
-                uint8_t* row_atom = staging + BM * ST_LDS * 2;
-                uint8_t* col_atom = row_atom + 512;
-                store_words16(p.a1 + m * p.f + n, p1);
-                store_words16(p.a3 + m * p.f + n, p3);
+                uint8_t* box = staging + (warp - 2) * C::FWD_BOX;
+                uint8_t* atoms = staging + EW * C::FWD_BOX + (acc_phase & 1) * 1024;  // row, then column atom
+                // this lane's row: 16-byte chunk k at k ^ ((row >> 1) & 3) (64B swizzle)
+                auto put_row = [&](const uint32_t* w) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(box + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                };
+                auto box_free = [&]() {  // the previous bulk store from the box has read it
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+                };
+                auto store_box = [&](const CUtensorMap* map) {
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(map, box, (int)n, (int)(m0 + q * 32));
+                        bulk_commit();
+                    }
+                };
+                box_free();
+                put_row(p1);
+                store_box(&tmX);
                 uint32_t hp[16];  // bf16x2 of h = bf16(fl32(SiLU(a1)) * a3)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -1253,46 +1297,59 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     }
                     hp[i] = bf16x2_rn(hv[0], hv[1]);
                 }
+                box_free();
+                put_row(p3);
+                store_box(&tmY);
                 if (p.tap0) store_words16(p.tap0 + m * p.f + n, hp);
+                if (p.amax_ws) {
+                    // the tap's maxima for the NVFP4 encode that follows: the
+                    // tile's 128-row strip, its 128-column strip, the tensor
+                    const uint32_t mw = warp_amax_words<16>(hp);
+                    if (lane == 0) {
+                        atomicMax(&p.amax_ws[1 + (m0 >> 7)], mw);
+                        atomicMax(&p.amax_ws[1 + (p.M >> 7) + (n0 >> 7)], mw);
+                        tensor_amax = max(tensor_amax, mw);
+                    }
+                }
                 if (p.quantize) {
                     uint4 pk;
                     const uint32_t sc = mx_words_rn(hp, pk);
                     *reinterpret_cast<uint4*>(p.q_row_codes + m * (p.f >> 1) + (n >> 1)) = pk;
-                    row_atom[atom_off(lr, half)] = (uint8_t)sc;
-                    store_words16(hs + lr * ST_LDS + oc, hp);
-                    epi_sync();
-                    if (!epi_ok) break;
-                    // column-facing view: stored row = output column, blocks
-                    // along the tokens; thread = (32-row block j, column c),
-                    // reading the column-pair words down the block (two
-                    // neighbouring threads share each word)
+                    atoms[atom_off(lr, half)] = (uint8_t)sc;
+                    // the block's h into the box, then each lane takes one
+                    // column (one stored row of Q_c(h)) down the 32 rows
+                    box_free();
+                    put_row(hp);
+                    __syncwarp();
+                    uint32_t w[16];
                     {
-                        const int c = et & 127, j = et >> 7;
-                        uint32_t w[32];
+                        const int k = lane >> 3, b = (lane & 7) * 2;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            w[i] = *reinterpret_cast<const uint32_t*>(&hs[(32 * j + i) * ST_LDS + (c & ~1)]);
-                        uint32_t m2 = 0;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
-                        uint4 pkc;
-                        const uint32_t scc = mx_lane_rn(w, c & 1, (c & 1) ? (m2 & 0xFFFF0000u) : (m2 << 16), pkc);
-                        *reinterpret_cast<uint4*>(p.q_col_codes + (n0 + c) * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pkc;
-                        col_atom[atom_off(c, j)] = (uint8_t)scc;
+                        for (int i = 0; i < 16; ++i) {
+                            const int r0 = 2 * i, r1 = 2 * i + 1;
+                            const uint32_t lo = *reinterpret_cast<const uint16_t*>(box + r0 * 64 + ((k ^ ((r0 >> 1) & 3)) << 4) + b);
+                            const uint32_t hi = *reinterpret_cast<const uint16_t*>(box + r1 * 64 + ((k ^ ((r1 >> 1) & 3)) << 4) + b);
+                            w[i] = lo | (hi << 16);
+                        }
                     }
+                    uint4 pkc;
+                    const uint32_t scc = mx_words_rn(w, pkc);
+                    const int c = oc + lane;
+                    *reinterpret_cast<uint4*>(p.q_col_codes + (n0 + c) * (p.M >> 1) + ((m0 + 32 * q) >> 1)) = pkc;
+                    atoms[512 + atom_off(c, q)] = (uint8_t)scc;
+                    // the tile's scale atoms (double-buffered by tile, so one
+                    // barrier per tile suffices)
                     epi_sync();
                     if (!epi_ok) break;
                     if (et < 32) {
                         const int64_t a = (m0 >> 7) * (p.f >> 7) + (n0 >> 7);
                         *reinterpret_cast<uint4*>(p.q_row_scales + a * 512 + et * 16) =
-                            *reinterpret_cast<const uint4*>(row_atom + et * 16);
+                            *reinterpret_cast<const uint4*>(atoms + et * 16);
                     } else if (et < 64) {
                         const int64_t a = (n0 >> 7) * (p.M >> 7) + (m0 >> 7);
                         *reinterpret_cast<uint4*>(p.q_col_scales + a * 512 + (et - 32) * 16) =
-                            *reinterpret_cast<const uint4*>(col_atom + (et - 32) * 16);
+                            *reinterpret_cast<const uint4*>(atoms + 512 + (et - 32) * 16);
                     }
-                    epi_sync();
                 }
             } else {
                 // EPI_SWIGLU_BWD: dh for output columns [oc, oc + 32) of this
@@ -1368,6 +1425,17 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     store_words16(p.tap1 + m * f2 + n, q1);
                     store_words16(p.tap1 + m * f2 + p.f + n, q3);
                 }
+                if (p.amax_ws) {
+                    // maxima of the [da1 | da3] tap: the tile's row strip
+                    // spans both, the column strips are da1's and da3's
+                    const uint32_t m1 = warp_amax_words<16>(q1), m3 = warp_amax_words<16>(q3);
+                    if (lane == 0) {
+                        atomicMax(&p.amax_ws[1 + (m0 >> 7)], max(m1, m3));
+                        atomicMax(&p.amax_ws[1 + (p.M >> 7) + (n0 >> 7)], m1);
+                        atomicMax(&p.amax_ws[1 + (p.M >> 7) + ((p.f + n0) >> 7)], m3);
+                        tensor_amax = max(tensor_amax, max(m1, m3));
+                    }
+                }
                 if (p.quantize) {
                     // row views of [da1 | da3] (stochastic rounding), one block each
                     uint4 pk;
@@ -1422,8 +1490,11 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
             }
             acc_phase ^= 1;
         }
+        if ((EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) && p.amax_ws && lane == 0 && tensor_amax)
+            atomicMax(&p.amax_ws[0], tensor_amax);
     }
-    if (is_store(EPI) && warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores done with shared memory
+    if ((is_store(EPI) || EPI == EPI_SWIGLU_FWD) && warp >= 2 && lane == 0)
+        bulk_wait_all();  // TMA stores done with shared memory
     if (Cfg<NV, BN, EPI, P2>::BWD_PREFETCH && warp >= 2 && warp < 2 + EW) cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
@@ -1515,12 +1586,17 @@ int sm_count() {
 template <bool NV, int BN, int EPI, int CM, bool P2 = false>
 int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream_t stream) {
     using C = Cfg<NV, BN, EPI, P2>;
-    CUtensorMap ta, tb, tc, tsa, tsb;
+    CUtensorMap ta, tb, tc, tsa, tsb, tx, ty;
     if (!make_map(&ta, g.a_codes, g.M, g.K) || !make_map(&tb, g.b_codes, g.b_rows, g.K, P2 ? BN / 2 : 128))
         return FP4_ERR_CUDA;
     memset(&tc, 0, sizeof tc);
     memset(&tsa, 0, sizeof tsa);
     memset(&tsb, 0, sizeof tsb);
+    memset(&tx, 0, sizeof tx);
+    memset(&ty, 0, sizeof ty);
+    if (EPI == EPI_SWIGLU_FWD && (!make_out_map(&tx, g.a1, g.M, g.f, FP4_OUT_BF16, 64) ||
+                                  !make_out_map(&ty, g.a3, g.M, g.f, FP4_OUT_BF16, 64)))
+        return FP4_ERR_CUDA;
     if (P2) {
         const int64_t k_atoms = NV ? g.K / 64 : g.K / 128;
         if (!make_sf_map(&tsa, g.a_scales, (g.M / 128) * k_atoms, C::SF_CHUNKS) ||
@@ -1576,7 +1652,7 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
         k.n_inner = n_inner ? 1 : 0;
         k.band = band < 1 ? 1 : (band > units ? units : band);
     }
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsa, tsb, k) != cudaSuccess) return FP4_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsa, tsb, tx, ty, k) != cudaSuccess) return FP4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -1619,6 +1695,7 @@ KParams kparams_of(const GemmParams& g) {
     p.rms_g = g.rms_g;
     p.rms_rstd = g.rms_rstd;
     p.rms_part = g.rms_part;
+    p.amax_ws = g.amax_ws;
     return p;
 }
 

@@ -37,6 +37,7 @@ struct QuantParams {
     const uint16_t* rp;    // r' (bwd)
     const uint16_t* dres;  // incoming residual gradient (bwd), may be NULL
     uint16_t* tap;         // bf16 [R][C] copy of the values quantized (NULL: not written)
+    int amax_ready;        // NVFP4: amax_ws already holds x's maxima (no pre-pass)
     //   PRE_ROPE_BWD     x = (dq, dk, dv) head-major [heads][R][128]; value = the
     //                    QKV-layout gradient [R][C], dq and dk turned back
     //                    (bf16(fl32(fl32(a c) + fl32(b s))), bf16(fl32(fl32(b c) - fl32(a s))))
@@ -51,6 +52,11 @@ enum { PRE_NONE = 0, PRE_RMSNORM_FWD = 1, PRE_RMSNORM_BWD = 2, PRE_ROPE_BWD = 3 
 
 int launch_rmsnorm_fwd_stats(const uint16_t* r, const uint16_t* b, int64_t R, int64_t C, int64_t ld, float eps,
                              uint16_t* r_out, float* rstd, cudaStream_t stream);
+// the same, and for an NVFP4 encode the maxima of y = bf16(r' * rstd * g)
+// folded into the quantizer's amax slots (zeroed by the caller)
+int launch_rmsnorm_fwd_stats_amax(const uint16_t* r, const uint16_t* b, const uint16_t* g, int64_t R, int64_t C,
+                                  int64_t ld, float eps, uint16_t* r_out, float* rstd, uint32_t* amax_ws,
+                                  cudaStream_t stream);
 int launch_rmsnorm_bwd_stats(const uint16_t* dy, const uint16_t* rp, const float* rstd, const uint16_t* g, int64_t R,
                              int64_t C, float* mean_g, cudaStream_t stream);
 // mean_g[row] = (sum over j in order of part[row][j]) / C
@@ -105,6 +111,10 @@ struct GemmParams {
     const uint16_t* rms_g;   // g bf16 [N]
     const float* rms_rstd;   // [M]
     float* rms_part;         // [M][N / 64], or NULL
+    // SwiGLU epilogues writing the bf16 tap for an NVFP4 encode: the tap's
+    // maxima folded into the quantizer's amax slots (tensor, row strips,
+    // column strips of the [M][f] or [M][2f] tensor), or NULL
+    uint32_t* amax_ws;
 };
 
 int launch_gemm(const GemmParams& p, cudaStream_t stream);

@@ -806,7 +806,7 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
     const bool nvr = (do_row ? p.row_route : p.col_route) != FP4_ROUTE_MXFP4;
     const bool nvc = (do_col ? p.col_route : p.row_route) != FP4_ROUTE_MXFP4;
     const size_t slots = quant_workspace_slots(p.R, p.C, p.row_route, p.col_route, p.views, p.flags);
-    if (slots) {
+    if (slots && !p.amax_ready) {
         if (cudaMemsetAsync(p.amax_ws, 0, slots * 4, stream) != cudaSuccess) return FP4_ERR_CUDA;
         const bool col_h16 = (p.flags & FP4_FLAG_HADAMARD16_COL) && do_col && p.col_route != FP4_ROUTE_MXFP4;
         if (p.pre != PRE_NONE || col_h16) {

@@ -34,7 +34,7 @@ import torch
 from . import (FP4_FLAG_SR_ROW, FP4_FLAG_WEIGHT_2D, FP4_OUT_BF16, FP4_VIEW_COL, FP4_VIEW_ROW, alloc_view,
                fp4_linear_dgrad, fp4_linear_dgrad_rmsnorm, fp4_linear_fprop, fp4_linear_wgrad, fp4_quantize,
                fp4_quantize_workspace_bytes, fp4_residual_rmsnorm_bwd_parts, fp4_residual_rmsnorm_fwd,
-               fp4_rmsnorm_bwd_workspace_bytes, fp4_swiglu_bwd, fp4_swiglu_fwd)
+               fp4_rmsnorm_bwd_workspace_bytes, fp4_swiglu_bwd, fp4_swiglu_fwd, fp4_swiglu_workspace_bytes)
 
 
 @dataclass
@@ -120,11 +120,12 @@ class FP4LinearStack:
             s["h"] = (alloc_view(r, T, f, 0, dev), alloc_view(r, f, T, 0, dev))
             s["f"] = torch.empty((T, d), **bf)
             ws_bytes = max(ws_bytes, fp4_quantize_workspace_bytes(r, T, q), fp4_quantize_workspace_bytes(r, T, 2 * f),
-                           fp4_rmsnorm_bwd_workspace_bytes(r, T, d))
+                           fp4_rmsnorm_bwd_workspace_bytes(r, T, d), fp4_swiglu_workspace_bytes(r, T, f, True, True),
+                           fp4_swiglu_workspace_bytes(r, T, f, False, True))
         self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         # scratch shared by all blocks (used strictly in sequence)
-        self.h_tap = torch.empty((T, f), **bf)       # NVFP4 SwiGLU: h before quantization
-        self.da13 = torch.empty((T, 2 * f), **bf)    # NVFP4 SwiGLU backward: [da1 | da3]
+        self.h_tap = torch.empty((T, f), **bf)       # NVFP4 SwiGLU: the bf16 copy of h the producer encodes
+        self.da13 = torch.empty((T, 2 * f), **bf)    # NVFP4 SwiGLU backward: the bf16 copy of [da1 | da3]
         self.dqkv = torch.zeros((T, q), **bf)        # attention stand-in gradient (K, V parts stay 0)
         self.dattn = torch.empty((T, d), **bf)
         self.dy = torch.empty((T, d), **bf)
@@ -162,11 +163,10 @@ class FP4LinearStack:
             fp4_linear_fprop(s["attn"][0], wv["o"][0], s["o"], FP4_OUT_BF16)
             fp4_residual_rmsnorm_fwd(s["r1"], s["o"], self.g2, r, 3, self.eps, r_out=s["r2"], rstd=s["rstd2"],
                                      y_row=s["y2"][0], y_col=s["y2"][1], workspace=self.ws)
-            if r == "mx":
-                fp4_swiglu_fwd(s["y2"][0], wv["w13"][0], f, a1=s["a1"], a3=s["a3"], h_row=s["h"][0], h_col=s["h"][1])
-            else:
-                fp4_swiglu_fwd(s["y2"][0], wv["w13"][0], f, a1=s["a1"], a3=s["a3"], h_tap=self.h_tap, quantize=False)
-                fp4_quantize(self.h_tap, r, 3, 0, row_out=s["h"][0], col_out=s["h"][1], workspace=self.ws)
+            # the views of h come from the producer for both routes (NVFP4
+            # through one bf16 copy of h whose maxima the epilogue folds)
+            fp4_swiglu_fwd(s["y2"][0], wv["w13"][0], f, a1=s["a1"], a3=s["a3"], h_row=s["h"][0], h_col=s["h"][1],
+                           h_tap=None if r == "mx" else self.h_tap, workspace=self.ws)
             fp4_linear_fprop(s["h"][0], wv["w2"][0], s["f"], FP4_OUT_BF16)
             h_prev, f_prev = s["r2"], s["f"]
         return h_prev, f_prev
@@ -186,13 +186,8 @@ class FP4LinearStack:
             off1, off2, off3, off4 = (sr_offset(st, i, k) for k in (1, 2, 3, 4))
             # FFN: W2 Wgrad, fused W2 Dgrad + SiLU derivative, W1/W3 Dgrad and Wgrad
             fp4_linear_wgrad(dF[1], s["h"][1], dw["w2"])
-            if r == "mx":
-                fp4_swiglu_bwd(dF[0], wv["w2"][1], f, s["a1"], s["a3"], sr_seed, off1, da13_row=gv["da13"][0],
-                               da13_col=gv["da13"][1])
-            else:
-                fp4_swiglu_bwd(dF[0], wv["w2"][1], f, s["a1"], s["a3"], da13_tap=self.da13, quantize=False)
-                fp4_quantize(self.da13, r, 3, FP4_FLAG_SR_ROW, sr_seed=sr_seed, sr_offset=off1,
-                             row_out=gv["da13"][0], col_out=gv["da13"][1], workspace=self.ws)
+            fp4_swiglu_bwd(dF[0], wv["w2"][1], f, s["a1"], s["a3"], sr_seed, off1, da13_row=gv["da13"][0],
+                           da13_col=gv["da13"][1], da13_tap=None if r == "mx" else self.da13, workspace=self.ws)
             fp4_linear_dgrad_rmsnorm(gv["da13"][0], wv["w13"][1], s["r2"], s["rstd2"], self.g2, dx=self.dy,
                                      part=self.part)
             fp4_linear_wgrad(gv["da13"][1], s["y2"][1], dw["w13"])

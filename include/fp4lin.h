@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define FP4LIN_VERSION 100 /* 1.0.0 */
+#define FP4LIN_VERSION 110 /* 1.1.0 */
 
 /* Exported symbols keep default visibility (the library builds with hidden
  * visibility for everything else). */
@@ -279,17 +279,25 @@ FP4_API int fp4_qkv_rope_bwd(int route, unsigned views, int sr, const void* dq, 
  *   a1 = X W1^T, a3 = X W3^T     (x_row: Q_r(X) [T][d]; w13_row: Q_r of the
  *                                 stacked [W1; W3] [2f][d], rows [0,f) = W1),
  * whose epilogue writes the retained BF16 values a1, a3 (device bf16
- * [T][f], the exact values autograd needs) and h = bf16(fl32(silu(a1)) * a3):
- *   MXFP4  h is emitted directly as Q_r(h) [T][f] (W2 Fprop input) and
- *          Q_c(h) [f][T] (W2 Wgrad input) into h_row / h_col;
- *   NVFP4  the outer factors of h need its full-strip maximum, so h is
- *          written to h_tap (required) and quantized with fp4_quantize;
- *          h_row / h_col must be NULL.
- * h_tap (device bf16 [T][f]) is optional for MXFP4.  T % 128 == 0,
- * f % 128 == 0, d % 256 == 0.  Errors: FP4_ERR_INVALID_ARG,
- * FP4_ERR_UNSUPPORTED_SHAPE, FP4_ERR_ROUTE_MISMATCH, FP4_ERR_CUDA. */
+ * [T][f], the exact values autograd needs) and h = bf16(fl32(silu(a1)) * a3),
+ * emitted as Q_r(h) [T][f] (the W2 Fprop input) and Q_c(h) [f][T] (the W2
+ * Wgrad input) into h_row / h_col (both or neither):
+ *   MXFP4  directly from the epilogue; workspace unused (may be NULL);
+ *   NVFP4  every outer factor of h needs its whole strip's maximum (all f
+ *          columns for the row view, all T tokens for the column view), so
+ *          h passes through one bf16 copy: the epilogue writes it and folds
+ *          its strip and tensor maxima into slots in `workspace`, then the
+ *          encoder reads it once (no separate maximum pass).  The copy is
+ *          h_tap when given, else it lives in the workspace;
+ *          fp4_swiglu_workspace_bytes gives the size (caller-owned device
+ *          memory, 16-byte aligned; FP4_ERR_WORKSPACE if smaller).
+ * With h_row = h_col = NULL only h_tap (device bf16 [T][f]) is written.
+ * T % 128 == 0, f % 128 == 0, d % 256 == 0.  Errors: FP4_ERR_INVALID_ARG,
+ * FP4_ERR_UNSUPPORTED_SHAPE, FP4_ERR_ROUTE_MISMATCH, FP4_ERR_WORKSPACE,
+ * FP4_ERR_CUDA. */
 FP4_API int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, int64_t f, void* a1, void* a3,
-                           fp4_tensor* h_row, fp4_tensor* h_col, void* h_tap, fp4_stream_t stream);
+                           fp4_tensor* h_row, fp4_tensor* h_col, void* h_tap, void* workspace,
+                           size_t workspace_bytes, fp4_stream_t stream);
 
 /* Fused gated-FFN backward producer (Sec. 3.2).  The W2 data-gradient
  * contraction dh = dY2 W2 (dy2_row: Q_r(dY2) [T][d]; w2_col: Q_c(W2) [f][d])
@@ -297,16 +305,26 @@ FP4_API int fp4_swiglu_fwd(const fp4_tensor* x_row, const fp4_tensor* w13_row, i
  * retained a1, a3 (device bf16 [T][f]):
  *   da1 = bf16(dh * a3 * s * (1 + a1 * (1 - s))),  da3 = bf16(dh * a1 * s),
  *   s = 1 / (1 + exp(-a1)),
- * laid out as one logical tensor da13 = [da1 | da3] of [T][2f]:
- *   MXFP4  emitted as Q_r(da13) [T][2f] with stochastic rounding (Philox
- *          under sr_seed / sr_offset, element index t * 2f + c; the W1/W3
- *          Dgrad operand, K = 2f) and Q_c(da13) [2f][T] (the W1/W3 Wgrad
- *          operand) into da13_row / da13_col;
- *   NVFP4  written to da13_tap (required) for fp4_quantize; views NULL.
- * dh_tap (bf16 [T][f]) and da13_tap (bf16 [T][2f]) are optional for MXFP4. */
+ * laid out as one logical tensor da13 = [da1 | da3] of [T][2f], emitted as
+ * Q_r(da13) [T][2f] with stochastic rounding (Philox under sr_seed /
+ * sr_offset, element index t * 2f + c; the W1/W3 Dgrad operand, K = 2f) and
+ * Q_c(da13) [2f][T] (the W1/W3 Wgrad operand) into da13_row / da13_col:
+ *   MXFP4  directly from the epilogue;
+ *   NVFP4  through one bf16 copy of da13 (da13_tap, else in the workspace)
+ *          whose maxima the epilogue folds, as for the forward
+ *          (fp4_swiglu_workspace_bytes with backward = 1).
+ * dh_tap (bf16 [T][f]) and da13_tap (bf16 [T][2f]) are optional debug
+ * copies; with da13_row = da13_col = NULL only the taps are written. */
 FP4_API int fp4_swiglu_bwd(const fp4_tensor* dy2_row, const fp4_tensor* w2_col, int64_t f, const void* a1,
                            const void* a3, uint64_t sr_seed, uint64_t sr_offset, fp4_tensor* da13_row,
-                           fp4_tensor* da13_col, void* dh_tap, void* da13_tap, fp4_stream_t stream);
+                           fp4_tensor* da13_col, void* dh_tap, void* da13_tap, void* workspace,
+                           size_t workspace_bytes, fp4_stream_t stream);
+
+/* Workspace bytes of the NVFP4 gated-FFN producers (0 for MXFP4): the
+ * maximum slots of the encoded tensor (h [T][f], or da13 [T][2f] when
+ * backward != 0), padded to 256 bytes, plus its bf16 copy unless with_tap
+ * (the caller passes h_tap / da13_tap).  Host only. */
+FP4_API int fp4_swiglu_workspace_bytes(int route, int64_t T, int64_t f, int backward, int with_tap, size_t* bytes);
 
 /* Residual + RMSNorm producer, forward (Sec. 3.2: the residual-RMSNorm
  * boundary retains the exact residual and its row statistics while producing

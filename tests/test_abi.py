@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
     L = F.load()
     missing = [n for n in declared_functions() if not hasattr(L, n)]
     assert not missing, missing
-    assert L.fp4_version() == 100
+    assert L.fp4_version() == 110
 
 
 def test_tensor_bytes():

@@ -34,6 +34,15 @@ def ordered(b):
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
+def same_views(a, b, what):
+    """Two GPU views of one tensor: codes, scales and outer factors equal."""
+    torch.cuda.synchronize()
+    assert torch.equal(a.codes, b.codes), f"{what}: codes"
+    assert torch.equal(a.scales, b.scales), f"{what}: scales"
+    if a.outer is not None or b.outer is not None:
+        assert torch.equal(a.outer[:a.outer_count], b.outer[:b.outer_count]), f"{what}: outer factors"
+
+
 def ulp(a, b):
     return np.abs(ordered(a) - ordered(b))
 
@@ -80,15 +89,21 @@ def test_swiglu_forward(route, T):
     d_h = ulp(g_h, o_h)[same_in]
     assert d_h.max() <= 1 and (d_h > 0).mean() < 0.01
     same_h = g_h == o_h
-    if route == "mx":
-        assert_view_masked(mhost(hr), oracle.quantize(o_h, "mx", "row"), g_h, same_h, "Q_r(h)")
-        assert_view_masked(mhost(hc), oracle.quantize(o_h, "mx", "col"), oriented(g_h, "col"),
-                           oriented(same_h, "col"), "Q_c(h)")
-    else:
-        assert hr is None and hc is None
+    assert_view_masked(mhost(hr), oracle.quantize(o_h, route, "row"), g_h, same_h, "Q_r(h)")
+    assert_view_masked(mhost(hc), oracle.quantize(o_h, route, "col"), oriented(g_h, "col"),
+                       oriented(same_h, "col"), "Q_c(h)")
+    if route != "mx":
+        # NVFP4: the maxima folded by the epilogue give exactly the encoding
+        # of the tap by the plain producer, with or without a caller's tap
+        qr, qc = F.fp4_quantize(tap, route, 3)
+        same_views(hr, qr, "Q_r(h) vs the producer on the tap")
+        same_views(hc, qc, "Q_c(h) vs the producer on the tap")
+        _, _, hr2, hc2 = F.fp4_swiglu_fwd(xr, wr, f)
+        same_views(hr2, hr, "Q_r(h) without a tap")
+        same_views(hc2, hc, "Q_c(h) without a tap")
 
 
-@pytest.mark.parametrize("route", ["mx", "nv_local"])
+@pytest.mark.parametrize("route", ["mx", "nv_global", "nv_local"])
 def test_swiglu_backward(route):
     T, d, f = 256, 256, 384
     dy2 = normal_bf16((T, d), 1e-2, 32, 1)
@@ -115,13 +130,17 @@ def test_swiglu_backward(route):
     dd = ulp(g_da, o_da)[same_dh]
     assert dd.max() <= 1 and (dd > 0).mean() < 0.01, "da13"
     same_da = g_da == o_da
-    if route == "mx":
-        assert_view_masked(mhost(rr), oracle.quantize(o_da, "mx", "row", sr=True, seed=77, offset=5), g_da,
-                           same_da, "Q_r(da13)")
-        assert_view_masked(mhost(cc), oracle.quantize(o_da, "mx", "col"), oriented(g_da, "col"),
-                           oriented(same_da, "col"), "Q_c(da13)")
-    else:
-        assert rr is None and cc is None
+    assert_view_masked(mhost(rr), oracle.quantize(o_da, route, "row", sr=True, seed=77, offset=5), g_da,
+                       same_da, "Q_r(da13)")
+    assert_view_masked(mhost(cc), oracle.quantize(o_da, route, "col"), oriented(g_da, "col"),
+                       oriented(same_da, "col"), "Q_c(da13)")
+    if route != "mx":
+        qr, qc = F.fp4_quantize(da_tap, route, 3, F.FP4_FLAG_SR_ROW, sr_seed=77, sr_offset=5)
+        same_views(rr, qr, "Q_r(da13) vs the producer on the tap")
+        same_views(cc, qc, "Q_c(da13) vs the producer on the tap")
+        rr2, cc2 = F.fp4_swiglu_bwd(dr, wc, f, to_dev(a1), to_dev(a3), sr_seed=77, sr_offset=5)
+        same_views(rr2, rr, "Q_r(da13) without a tap")
+        same_views(cc2, cc, "Q_c(da13) without a tap")
 
 
 def test_swiglu_chain_matches_unfused_path():
