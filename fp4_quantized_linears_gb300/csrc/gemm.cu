@@ -650,11 +650,14 @@ struct Cfg {
     // SwiGLU forward: one 2 KB box (32 rows x 64 bytes) per epilogue warp,
     // and the row and column scale atoms of two tiles
     static constexpr int FWD_BOX = 32 * 64;
+    // SwiGLU backward: one 2 KB box per epilogue warp for its column views,
+    // the four scale atoms (row da1, row da3, column da1, column da3) of two
+    // tiles, and the a1 / a3 prefetch slots
     static constexpr int STAGING =
         is_store(EPI)          ? EPI_WARPS * OUT_BUFS * OUT_BOX
         : EPI == EPI_QKV_ROPE  ? 0
         : EPI == EPI_SWIGLU_FWD ? epi_warps(EPI) * FWD_BOX + 4 * 512
-                               : 2 * BM * ST_LDS * 2 + 4 * 512 + PREFETCH_BYTES;
+                               : epi_warps(EPI) * FWD_BOX + 2 * 4 * 512 + PREFETCH_BYTES;
     static constexpr int STAGES = fit(STAGING);
     static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + RESERVED;
     static_assert(STAGES >= 3, "pipeline depth");
@@ -1009,7 +1012,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         // 16-byte chunk i (a1: 0-3, a3: 4-7) of epilogue thread et sits at
         // (i * 32 * EW + et) * 16, so a warp's accesses to one chunk are 512
         // contiguous bytes (no bank conflicts).
-        const uint32_t slot = smem_u32(staging + 2 * BM * ST_LDS * 2 + 4 * 512) + (uint32_t)et * 16;
+        const uint32_t slot = smem_u32(staging + EW * C::FWD_BOX + 2 * 4 * 512) + (uint32_t)et * 16;
         constexpr uint32_t CHUNK_STRIDE = 32 * EW * 16;
         auto prefetch_a13 = [&](int64_t u2) {
             if constexpr (C::BWD_PREFETCH) {
@@ -1370,9 +1373,9 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     for (int i = 0; i < 16; ++i)
                         dp[i] = bf16x2_rn(__uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
                 }
-                uint16_t* s1 = reinterpret_cast<uint16_t*>(staging);
-                uint16_t* s3 = s1 + BM * ST_LDS;
-                uint8_t* atoms = staging + 2 * BM * ST_LDS * 2;  // row da1, row da3, col da1, col da3
+                uint8_t* box = staging + (warp - 2) * C::FWD_BOX;
+                // row da1, row da3, column da1, column da3; double-buffered by tile
+                uint8_t* atoms = staging + EW * C::FWD_BOX + (acc_phase & 1) * 2048;
                 const int64_t f2 = 2 * p.f;
                 if (p.tap0) store_words16(p.tap0 + m * p.f + n, dp);
                 // da1 = bf16(dh * a3 * SiLU'(a1)), da3 = bf16(dh * SiLU(a1)), as bf16x2 words
@@ -1381,7 +1384,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     uint4 v1[4], v3[4];
                     if constexpr (C::BWD_PREFETCH) {
                         cp_async_wait_all();  // this thread's own copies of this tile's segments
-                        const uint8_t* s13 = staging + 2 * BM * ST_LDS * 2 + 4 * 512 + et * 16;
+                        const uint8_t* s13 = staging + EW * C::FWD_BOX + 2 * 4 * 512 + et * 16;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             v1[i] = *reinterpret_cast<const uint4*>(s13 + i * CHUNK_STRIDE);
@@ -1445,34 +1448,37 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                     sc = mx_words_sr(q3, (uint64_t)(m * f2 + p.f + n) >> 3, p.sr_keys, p.offset, pk);
                     *reinterpret_cast<uint4*>(p.q_row_codes + m * p.f + ((p.f + n) >> 1)) = pk;
                     atoms[512 + atom_off(lr, half)] = (uint8_t)sc;
-                    store_words16(s1 + lr * ST_LDS + oc, q1);
-                    store_words16(s3 + lr * ST_LDS + oc, q3);
-                    epi_sync();
-                    if (!epi_ok) break;
-                    // column views: thread = (da1 or da3, 32-row block j, column
-                    // pair cp); it reads 32 bf16x2 words down the pair (one 32-bit
-                    // load per two values) and encodes both columns
-                    {
-                        const int which = et >> 8, j = (et >> 6) & 3, cp = et & 63;
-                        const uint16_t* src = which ? s3 : s1;
-                        uint32_t w[32];
+                    // column views: this warp's 32 x 32 block of da1, then of
+                    // da3, through its box (64B swizzle); each lane encodes
+                    // one column (one stored row of Q_c(da13)) down the block
+#pragma unroll 1
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t* src = which ? q3 : q1;
+                        __syncwarp();  // the previous reads of the box are done
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            w[i] = *reinterpret_cast<const uint32_t*>(&src[(32 * j + i) * ST_LDS + 2 * cp]);
-                        uint32_t m2 = 0;
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<uint4*>(box + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(src[4 * k], src[4 * k + 1], src[4 * k + 2], src[4 * k + 3]);
+                        __syncwarp();
+                        uint32_t w[16];
+                        const int ck = lane >> 3, cb = (lane & 7) * 2;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            m2 = __vimax3_u16x2(m2, w[i] & 0x7FFF7FFFu, w[i + 1] & 0x7FFF7FFFu);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int cidx = 2 * cp + h;
-                            uint4 pkc;
-                            const uint32_t scc = mx_lane_rn(w, h, h ? (m2 & 0xFFFF0000u) : (m2 << 16), pkc);
-                            const int64_t srow = (which ? p.f : 0) + n0 + cidx;
-                            *reinterpret_cast<uint4*>(p.q_col_codes + srow * (p.M >> 1) + ((m0 + 32 * j) >> 1)) = pkc;
-                            atoms[1024 + which * 512 + atom_off(cidx, j)] = (uint8_t)scc;
+                        for (int i = 0; i < 16; ++i) {
+                            const int r0 = 2 * i, r1 = 2 * i + 1;
+                            const uint32_t lo =
+                                *reinterpret_cast<const uint16_t*>(box + r0 * 64 + ((ck ^ ((r0 >> 1) & 3)) << 4) + cb);
+                            const uint32_t hi =
+                                *reinterpret_cast<const uint16_t*>(box + r1 * 64 + ((ck ^ ((r1 >> 1) & 3)) << 4) + cb);
+                            w[i] = lo | (hi << 16);
                         }
+                        uint4 pkc;
+                        const uint32_t scc = mx_words_rn(w, pkc);
+                        const int64_t srow = (which ? p.f : 0) + n + lane;
+                        *reinterpret_cast<uint4*>(p.q_col_codes + srow * (p.M >> 1) + ((m0 + 32 * q) >> 1)) = pkc;
+                        atoms[1024 + which * 512 + atom_off(oc + lane, q)] = (uint8_t)scc;
                     }
+                    // the tile's four scale atoms (double-buffered by tile, so
+                    // one barrier per tile suffices)
                     epi_sync();
                     if (!epi_ok) break;
                     if (et < 128) {
@@ -1485,7 +1491,6 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                         uint8_t* dst = (which < 2 ? p.q_row_scales : p.q_col_scales) + a * 512 + part * 16;
                         *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(atoms + which * 512 + part * 16);
                     }
-                    epi_sync();
                 }
             }
             acc_phase ^= 1;
