@@ -121,33 +121,63 @@ FP4_DEV float max3_abs_nan(float m, float a, float b) {
 // SAT: saturate at code 7 (|v| >= 6).  Without it the caller guarantees
 // |v| <= 6, as an MXFP4 block under its upward scale does (6 * 2^e >= amax,
 // and scaling by 2^-e is exact); then b <= 6 and the code is at most 7.
+//
+// The encoders are bound by the integer ALU pipe, so the addends
+// 2^22 - 1 - u * 2^6 - 0x3F000000 (mod 2^32) are formed as u * -64 + K by
+// the integer multiply-add, which issues to the multiply-add pipe instead,
+// and the sign bits of 8 values are gathered once per code word by byte
+// permutes (prmt with the sign-replicating selector nibbles 8-15).
+FP4_DEV uint32_t mad_lo_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+FP4_DEV uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
 template <bool SAT = true>
 FP4_DEV uint32_t sr_code_pair(float ax, float ay, uint32_t rw) {
+    constexpr uint32_t K = 0x3FFFFFu - 0x3F000000u;
     float cx, cy;
     f32x2_fma_rp(cx, cy, ax, ay, 0.5f, 0.5f, 0.5f, 0.5f);  // fl_up((|v| + 1) / 2)
     const uint32_t tx = max(__float_as_uint(ax), __float_as_uint(cx));
     const uint32_t ty = max(__float_as_uint(ay), __float_as_uint(cy));
-    uint32_t hx = (tx + (((rw << 6) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22;
-    uint32_t hy = (ty + (((rw >> 10) & 0x3FFFC0u) ^ 0x3FFFFFu) - 0x3F000000u) >> 22;
+    uint32_t hx = (tx + mad_lo_u32(rw & 0xFFFFu, 0xFFFFFFC0u, K)) >> 22;
+    uint32_t hy = (ty + mad_lo_u32(rw >> 16, 0xFFFFFFC0u, K)) >> 22;
     if (SAT) {
         hx = min(hx, 7u);
         hy = min(hy, 7u);
     }
     return hx | (hy << 4);
 }
-FP4_DEV uint32_t e2m1x2_sr(float x, float y, uint32_t rw) {
-    const uint32_t bx = __float_as_uint(x), by = __float_as_uint(y);
-    return sr_code_pair(fabsf(x), fabsf(y), rw) | ((bx >> 28) & 8u) | ((by >> 24) & 0x80u);
+// The sign bits of the 8 bf16 values of 4 words (word b: values 2b low half,
+// 2b + 1 high half) at the sign positions 4k + 3 of a word of 8 codes: the
+// high bytes of the halves (bytes 1 and 3 of each word) are collected, the
+// even values' bytes and the odd values' bytes each sign-replicated into one
+// word, and nibble k takes its sign from the matching one.
+FP4_DEV uint32_t e2m1x8_signs(const uint32_t* w) {
+    const uint32_t p01 = prmt_b32(w[0], w[1], 0x7351u), p23 = prmt_b32(w[2], w[3], 0x7351u);
+    const uint32_t even = prmt_b32(p01, p23, 0xDC98u), odd = prmt_b32(p01, p23, 0xFEBAu);
+    return ((even & 0x0F0F0F0Fu) | (odd & 0xF0F0F0F0u)) & 0x88888888u;
 }
-// The two bf16 values of one word (low half first) scaled by a non-negative
-// multiplier (fl32(x * mult), as the RN path) and rounded stochastically; the
-// codes keep the inputs' sign bits.
+// The 8 bf16 values of 4 words scaled by a non-negative multiplier
+// (fl32(x * mult), as the RN path) and rounded stochastically with the 16-bit
+// uniforms of rb (word b: value 2b low half, 2b + 1 high half); the codes keep
+// the inputs' sign bits.
 template <bool SAT = true>
-FP4_DEV uint32_t e2m1x2_sr_bf16(uint32_t w, float mult, uint32_t rw) {
-    const uint32_t wa = w & 0x7FFF7FFFu;
-    float ax, ay;
-    f32x2_mul(ax, ay, __uint_as_float(wa << 16), __uint_as_float(wa & 0xFFFF0000u), mult, mult);
-    return sr_code_pair<SAT>(ax, ay, rw) | ((w >> 12) & 8u) | ((w >> 24) & 0x80u);
+FP4_DEV uint32_t e2m1x8_sr_bf16(const uint32_t* w, float mult, uint4 rb) {
+    const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
+    uint32_t word = e2m1x8_signs(w);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t wa = w[b] & 0x7FFF7FFFu;
+        float ax, ay;
+        f32x2_mul(ax, ay, __uint_as_float(wa << 16), __uint_as_float(wa & 0xFFFF0000u), mult, mult);
+        word |= sr_code_pair<SAT>(ax, ay, rw[b]) << (8 * b);
+    }
+    return word;
 }
 
 // --------------------------------------------------------------- E4M3 ------

@@ -470,14 +470,7 @@ FP4_DEV uint32_t mx_words_sr(const uint32_t* w, uint64_t g0, const uint32_t* rk,
     const float mult = exp2_neg(e);
     uint32_t out[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 rb = sr_bits8(g0 + q, rk, offset);
-        const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16<false>(w[4 * q + b], mult, rw[b]) << (8 * b);
-        out[q] = word;
-    }
+    for (int q = 0; q < 4; ++q) out[q] = e2m1x8_sr_bf16<false>(w + 4 * q, mult, sr_bits8(g0 + q, rk, offset));
     packed = make_uint4(out[0], out[1], out[2], out[3]);
     return (uint32_t)(e + 127);
 }
@@ -635,14 +628,15 @@ struct Cfg {
     static constexpr int fit(int staging) {
         return cmin(MAX_STAGES, cmin((SMEM_LIMIT - RESERVED - staging) / STAGE_BYTES, (TMEM_COLS - SF_COL0) / SF_COLS));
     }
-    // STORE: each epilogue warp stages 32-row boxes for TMA stores: 128-byte
-    // rows where that costs the ring no stage, else 64-byte rows (twice the
-    // stores); two buffers per warp where the second costs no stage either
-    static constexpr int MAX_STAGES_OUT = fit(EPI_WARPS * 2048);
-    static constexpr int OUT_ROW = fit(EPI_WARPS * 4096) >= MAX_STAGES_OUT ? 128 : 64;  // bytes per box row
+    // STORE: each epilogue warp stages its rows in one buffer of 32 rows x
+    // 32 bytes (one sector per row) and writes it with a TMA store.  Of the
+    // box widths (16 to 128 bytes per row, one or two buffers) this is the
+    // fastest: the operand loads share the SM's TMA unit with these stores,
+    // and short stores hold it up least, while 16-byte rows write half
+    // sectors; pacing the stores over the tile gains nothing.
+    static constexpr int OUT_ROW = 32;  // bytes per box row
     static constexpr int OUT_BOX = 32 * OUT_ROW;
-    static constexpr int OUT_BUFS =
-        !is_store(EPI) ? 0 : (fit(EPI_WARPS * 2 * OUT_BOX) >= MAX_STAGES_OUT ? 2 : 1);
+    static constexpr int OUT_BUFS = is_store(EPI) ? 1 : 0;
     // SwiGLU backward on CTA pairs: each epilogue thread's retained a1 / a3
     // row segments (2 x 64 bytes) of the next tile land in a slot of its own
     static constexpr bool BWD_PREFETCH = EPI == EPI_SWIGLU_BWD && P2;
@@ -1079,14 +1073,9 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
 #pragma unroll
                     for (int bi = 0; bi < NB; ++bi) {
                         if (bi >= nbox) break;
-                        uint8_t* buf = wbuf + (C::OUT_BUFS == 2 ? (bi & 1) * C::OUT_BOX : 0);
+                        uint8_t* buf = wbuf;
                         // the store previously issued from this buffer must have read it
-                        if (lane == 0) {
-                            if (C::OUT_BUFS == 2)
-                                bulk_wait_read<1>();
-                            else
-                                bulk_wait_read<0>();
-                        }
+                        if (lane == 0) bulk_wait_read<0>();
                         __syncwarp();
                         const int cols = f32 ? WORDS : 2 * WORDS;
                         const int64_t n = n0 + half * (BN / 2) + cols * bi;
@@ -1126,11 +1115,12 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                                 }
                             }
                         }
-                        // this lane's row: 16-byte chunk k lands at k ^ (row & 7)
-                        // (128B swizzle) or k ^ ((row >> 1) & 3) (64B swizzle)
+                        // this lane's row: 16-byte chunk k lands at k ^ ((row >> 2) & 1)
+                        // (32B swizzle: no bank conflicts across the 8 lanes of a phase)
+                        static_assert(ROW == 32, "box row width");
 #pragma unroll
                         for (int k = 0; k < ROW / 16; ++k) {
-                            const int sw = ROW == 128 ? (lane & 7) : ((lane >> 1) & 3);
+                            const int sw = (lane >> 2) & 1;
                             *reinterpret_cast<uint4*>(buf + lane * ROW + ((k ^ sw) << 4)) =
                                 make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
                         }
@@ -1559,8 +1549,8 @@ bool make_sf_map(CUtensorMap* map, const void* scales, int64_t atoms, int chunk)
     return r == CUDA_SUCCESS;
 }
 
-// Row-major output [M][N] (fp32 or bf16), box `row_bytes` (128 or 64) x 32
-// rows with the swizzle of that width.
+// Row-major output [M][N] (fp32 or bf16), box `row_bytes` (128, 64 or 32) x
+// 32 rows with the swizzle of that width.
 bool make_out_map(CUtensorMap* map, void* c, int64_t M, int64_t N, int out_dtype, int row_bytes) {
     const bool f32 = out_dtype == FP4_OUT_F32;
     const int es = f32 ? 4 : 2;
@@ -1570,7 +1560,9 @@ bool make_out_map(CUtensorMap* map, void* c, int64_t M, int64_t N, int out_dtype
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_32B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -59,6 +59,17 @@ struct SmemQ {
 FP4_DEV int col_stage_off(int c, int j) { return j * 2048 + ((c ^ j) << 4); }
 
 // Byte offset of local block j (0..nb-1) of local row r in staged atoms.
+// Row segments: work item idx (0 .. 511) is 32-value segment j of local row
+// r, numbered so that the 8 lanes of each 16-byte shared-load phase read 8
+// consecutive rows at the same j (the padded row stride then spreads them
+// over all 32 banks; four segments of one row would pair up 128 bytes apart).
+FP4_DEV int seg_row(int idx) { return (idx & 7) + 8 * (idx >> 5); }
+FP4_DEV int seg_j(int idx) { return (idx >> 3) & 3; }
+// Row-view code staging: segment j of row r at chunk j ^ ((r >> 1) & 3), so
+// that both the encoders (8 rows, one j) and the write-out (2 rows, all four
+// chunks) touch every bank once per phase.
+FP4_DEV int row_stage_off(int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); }
+
 FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
 
 // fp32 bits of max |v[i]| over n values (non-negative, so the float and the
@@ -106,15 +117,7 @@ template <bool SAT>
 FP4_DEV uint4 pack_sr32(const uint32_t* w, float m0, float m1, uint64_t g0, const uint32_t* rk, uint64_t offset) {
     uint32_t out[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 rb = sr_bits8(g0 + q, rk, offset);
-        const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
-        const float mult = q < 2 ? m0 : m1;
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) word |= e2m1x2_sr_bf16<SAT>(w[4 * q + b], mult, rw[b]) << (8 * b);
-        out[q] = word;
-    }
+    for (int q = 0; q < 4; ++q) out[q] = e2m1x8_sr_bf16<SAT>(w + 4 * q, q < 2 ? m0 : m1, sr_bits8(g0 + q, rk, offset));
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
@@ -368,7 +371,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
     if (w2d) {
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {
-            const int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
+            const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
             const uint16_t* src = &tbuf[r * LDS + j * 32];
             uint32_t w[16];
 #pragma unroll
@@ -423,7 +426,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
         const bool sr = (p.flags & FP4_FLAG_SR_ROW) != 0;
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {
-            const int idx = t + k * THREADS, r = idx >> 2, j = idx & 3;
+            const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
             uint32_t w[16];
             const uint16_t* src = &tbuf[r * LDS + j * 32];
 #pragma unroll
@@ -466,7 +469,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 }
                 packed = pack_rn32(v, m0, m1);
             }
-            *reinterpret_cast<uint4*>(&s.row_codes[r * 64 + j * 16]) = packed;
+            *reinterpret_cast<uint4*>(&s.row_codes[row_stage_off(r, j)]) = packed;
         }
     }
 
@@ -540,7 +543,7 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
         for (int k = 0; k < 2; ++k) {
             int q = t + k * THREADS, rr = q >> 2, part = q & 3;
             *reinterpret_cast<uint4*>(p.row_codes + (r0 + rr) * (p.C >> 1) + (c0 >> 1) + part * 16) =
-                *reinterpret_cast<const uint4*>(&s.row_codes[rr * 64 + part * 16]);
+                *reinterpret_cast<const uint4*>(&s.row_codes[row_stage_off(rr, part)]);
         }
         const int nat = NVR ? 2 : 1;
         if (t < nat * 32) {

@@ -6,7 +6,10 @@ GPU parity tests then compare the kernels themselves with the oracle):
   Eq. 9) by a carry into the grid bit: b = max(|v|, fl_up((|v| + 1) / 2)),
   code = (bits(b) + 2^22 - 1 - u * 2^6 - 0x3F000000) >> 22, saturated at 7;
   compared with the oracle's rule (round up iff u / 2^16 < p) on values at,
-  next to and between every 2^-16 step of every grid interval;
+  next to and between every 2^-16 step of every grid interval; the kernels
+  form the addend as the 32-bit multiply-add u * (2^32 - 64) + K and gather
+  the 8 sign bits of a code word with byte permutes, both checked here
+  against the plain forms;
 * fl32(a / 6) of a bf16 block maximum (the NVFP4 scale, Sec. 2.2.2) as
   RN(q + RN(a - 6 q) * c), q = RN(a * c), c = RN(1 / 6), compared with the
   correctly rounded quotient for every finite positive bf16 value.
@@ -93,3 +96,41 @@ def test_division_by_six_is_correctly_rounded_for_every_bf16():
         q = rn32(a * c)
         r = rn32(a - 6 * q)
         assert rn32(q + r * c) == rn32(a / 6), hex(b)
+
+
+def prmt(a: int, b: int, sel: int) -> int:
+    """prmt.b32 in its default mode: byte n of d is byte (sel_n & 7) of the
+    8 bytes {b, a}, or that byte's sign replicated when sel_n & 8."""
+    src = [(a >> (8 * i)) & 0xFF for i in range(4)] + [(b >> (8 * i)) & 0xFF for i in range(4)]
+    d = 0
+    for n in range(4):
+        s = (sel >> (4 * n)) & 0xF
+        byte = src[s & 7]
+        if s & 8:
+            byte = 0xFF if byte & 0x80 else 0
+        d |= byte << (8 * n)
+    return d
+
+
+def test_sr_addend_multiply_add_form():
+    rng = np.random.default_rng(3)
+    k = (0x3FFFFF - 0x3F000000) & 0xFFFFFFFF
+    words = [0, 0xFFFFFFFF, 0xFFFF, 0xFFFF0000] + [int(x) for x in rng.integers(0, 2**32, 20000, dtype=np.uint64)]
+    for rw in words:
+        for u in (rw & 0xFFFF, rw >> 16):
+            plain = ((((u << 6) & 0x3FFFC0) ^ 0x3FFFFF) - 0x3F000000) & 0xFFFFFFFF
+            assert (u * 0xFFFFFFC0 + k) & 0xFFFFFFFF == plain, hex(rw)
+
+
+def test_sign_gather_by_byte_permutes():
+    rng = np.random.default_rng(4)
+    for _ in range(20000):
+        w = [int(x) for x in rng.integers(0, 2**32, 4, dtype=np.uint64)]
+        p01, p23 = prmt(w[0], w[1], 0x7351), prmt(w[2], w[3], 0x7351)
+        even, odd = prmt(p01, p23, 0xDC98), prmt(p01, p23, 0xFEBA)
+        got = ((even & 0x0F0F0F0F) | (odd & 0xF0F0F0F0)) & 0x88888888
+        want = 0
+        for b in range(4):  # value 2b: bit 15 of word b -> bit 8b + 3; value 2b + 1: bit 31 -> 8b + 7
+            want |= ((w[b] >> 15) & 1) << (8 * b + 3)
+            want |= ((w[b] >> 31) & 1) << (8 * b + 7)
+        assert got == want
