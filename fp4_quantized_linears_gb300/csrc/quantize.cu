@@ -15,10 +15,15 @@
 // NVFP4 first runs a tile-amax pre-pass (the tensor-wide / strip-wide maximum
 // that the outer factors need), so its algorithmic traffic is two reads.
 //
-// Memory behaviour: coalesced 16-byte loads of the tile into shared memory,
-// per-thread 32-value segments for both orientations read from shared memory,
-// codes and scale atoms staged in shared memory and written with coalesced
-// 16-byte stores (each tile's scale bytes form whole 512-byte atoms).
+// Memory behaviour: persistent CTAs, two per SM, each with a ring of three
+// tile slots filled by 16-byte cp.async copies two tiles ahead of the one
+// being encoded (about 128 KB in flight per SM); per-thread 32-value
+// segments for both orientations read from shared memory; codes stored from
+// registers (row view: the four 16-byte pieces of a row's 64 bytes from
+// adjacent lanes; column view: 16-byte pieces whose sector halves come from
+// neighbouring warps and merge in L2); scale atoms staged in shared memory and
+// written with coalesced 16-byte stores (each tile's scale bytes form whole
+// 512-byte atoms).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -38,10 +43,10 @@ constexpr int PAD = 8;               // bf16 elements of padding per smem row
 constexpr int LDS = TILE + PAD;      // smem row stride (elements)
 constexpr int THREADS = 256;
 
+constexpr int SLOTS = 3;             // tile ring: the tile being encoded and the next two landing
+
 struct SmemQ {
-    uint16_t tile[2][TILE * LDS];    // 2 x 34,816 B: the tile being encoded and the next one landing
-    uint8_t row_codes[TILE * 64];    // 8 KB staged row-view codes
-    uint8_t col_codes[TILE * 64];    // 8 KB staged column-view codes
+    uint16_t tile[SLOTS][TILE * LDS];  // 3 x 34,816 B
     uint8_t row_sc[1024];            // staged scale atoms (1 MX / 2 NV)
     uint8_t col_sc[1024];
     int tile_e[16];                  // 2D32: per 32x32 tile exponent
@@ -52,11 +57,6 @@ struct SmemQ {
     uint32_t red[THREADS / 32];
 };
 
-// Column-view code staging is segment-major with the stored row XOR-ed by the
-// segment index, so that both the encoding threads (consecutive stored rows)
-// and the write-out threads (four segments of a row) hit at most two lanes
-// per bank.
-FP4_DEV int col_stage_off(int c, int j) { return j * 2048 + ((c ^ j) << 4); }
 
 // Byte offset of local block j (0..nb-1) of local row r in staged atoms.
 // Row segments: work item idx (0 .. 511) is 32-value segment j of local row
@@ -65,10 +65,6 @@ FP4_DEV int col_stage_off(int c, int j) { return j * 2048 + ((c ^ j) << 4); }
 // over all 32 banks; four segments of one row would pair up 128 bytes apart).
 FP4_DEV int seg_row(int idx) { return (idx & 7) + 8 * (idx >> 5); }
 FP4_DEV int seg_j(int idx) { return (idx >> 3) & 3; }
-// Row-view code staging: segment j of row r at chunk j ^ ((r >> 1) & 3), so
-// that both the encoders (8 rows, one j) and the write-out (2 rows, all four
-// chunks) touch every bank once per phase.
-FP4_DEV int row_stage_off(int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); }
 
 FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
 
@@ -366,19 +362,25 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
         __syncthreads();  // the multiplier tables
     }
 
+    // 16-byte shared loads of this thread's row segment k (steps 2 and 3)
+    auto load_segment = [&](int k, uint32_t* w) {
+        const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
+        const uint16_t* src = &tbuf[r * LDS + j * 32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
+            w[4 * q] = d.x; w[4 * q + 1] = d.y; w[4 * q + 2] = d.z; w[4 * q + 3] = d.w;
+        }
+    };
+
     // 2. shared 2D weight scales: the maxima of the 16-value pieces of every
     //    row (16-byte shared loads), then one reduction per tile
     if (w2d) {
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {
             const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
-            const uint16_t* src = &tbuf[r * LDS + j * 32];
             uint32_t w[16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
-                w[4 * q] = d.x; w[4 * q + 1] = d.y; w[4 * q + 2] = d.z; w[4 * q + 3] = d.w;
-            }
+            load_segment(k, w);
             const uint32_t a0 = amax_words<8>(w), a1 = amax_words<8>(w + 8);
             s.seg_amax[r * 8 + 2 * j] = max(lane_lo_f32bits(a0), lane_hi_f32bits(a0));
             s.seg_amax[r * 8 + 2 * j + 1] = max(lane_lo_f32bits(a1), lane_hi_f32bits(a1));
@@ -424,16 +426,8 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
     // 3. row-facing view: segment (r, j) = 32 values of local row r starting at 32 j
     if (do_row) {
         const bool sr = (p.flags & FP4_FLAG_SR_ROW) != 0;
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
+        auto row_segment = [&](int k, const uint32_t* w) {
             const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
-            uint32_t w[16];
-            const uint16_t* src = &tbuf[r * LDS + j * 32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
-                w[4 * q] = d.x; w[4 * q + 1] = d.y; w[4 * q + 2] = d.z; w[4 * q + 3] = d.w;
-            }
             float m0, m1;
             if (w2d) {
                 if (!NVR) {
@@ -469,7 +463,13 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 }
                 packed = pack_rn32(v, m0, m1);
             }
-            *reinterpret_cast<uint4*>(&s.row_codes[row_stage_off(r, j)]) = packed;
+            *reinterpret_cast<uint4*>(p.row_codes + (r0 + r) * (p.C >> 1) + (c0 >> 1) + j * 16) = packed;
+        };
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            uint32_t w[16];
+            load_segment(k, w);
+            row_segment(k, w);
         }
     }
 
@@ -532,19 +532,13 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                 segment_scale<NVC>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1,
                                    NVC ? s.mtab[1] : nullptr);
             }
-            *reinterpret_cast<uint4*>(&s.col_codes[col_stage_off(c, j)]) = pack_rn32(v, m0, m1);
+            *reinterpret_cast<uint4*>(p.col_codes + (c0 + c) * (p.R >> 1) + (r0 >> 1) + j * 16) = pack_rn32(v, m0, m1);
         }
     }
     __syncthreads();
 
-    // 5. coalesced write-out of staged codes and scale atoms
+    // 5. coalesced write-out of the staged scale atoms
     if (do_row) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            int q = t + k * THREADS, rr = q >> 2, part = q & 3;
-            *reinterpret_cast<uint4*>(p.row_codes + (r0 + rr) * (p.C >> 1) + (c0 >> 1) + part * 16) =
-                *reinterpret_cast<const uint4*>(&s.row_codes[row_stage_off(rr, part)]);
-        }
         const int nat = NVR ? 2 : 1;
         if (t < nat * 32) {
             int64_t atoms_per_rowblock = NVR ? (p.C >> 6) : (p.C >> 7);
@@ -554,12 +548,6 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
         }
     }
     if (do_col) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            int q = t + k * THREADS, cc = q >> 2, part = q & 3;
-            *reinterpret_cast<uint4*>(p.col_codes + (c0 + cc) * (p.R >> 1) + (r0 >> 1) + part * 16) =
-                *reinterpret_cast<const uint4*>(&s.col_codes[col_stage_off(cc, part)]);
-        }
         const int nat = NVC ? 2 : 1;
         if (t < nat * 32) {
             int64_t atoms_per_rowblock = NVC ? (p.R >> 6) : (p.R >> 7);
@@ -577,7 +565,9 @@ FP4_DEV void cp_async16(void* dst, const void* src) {
                  : "memory");
 }
 FP4_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-FP4_DEV void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// all but the newest N groups of this thread's copies have landed
+template <int N>
+FP4_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Start loading the 128x128 tile at (r0, c0) into `tile` (row stride LDS).
 FP4_DEV void prefetch_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* tile) {
@@ -590,9 +580,11 @@ FP4_DEV void prefetch_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_
 }
 
 // Each CTA walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... (row-strip-major
-// order) with two tile buffers: while one tile is encoded the next one is
-// already in flight, so its load latency hides behind the encoding.  With an
-// RMSNorm pre-op the tile is loaded (and transformed) synchronously.
+// order) through a ring of three tile slots: while one tile is encoded the
+// next two are in flight (one commit group per tile, possibly empty), so the
+// load latency hides behind two tiles' encoding.  Slot (it + 2) % 3 is
+// refilled only after the barrier that ends tile it - 1, its last reader.
+// With an RMSNorm pre-op the tile is loaded (and transformed) synchronously.
 template <bool NVR, bool NVC>
 __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(const __grid_constant__ QuantParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -602,23 +594,28 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(const __grid_
     int64_t tile = blockIdx.x;
     if (tile >= n_tiles) return;
     if (async) {
-        prefetch_tile(p, (tile / tiles_x) * TILE, (tile % tiles_x) * TILE, s.tile[0]);
-        cp_async_commit();
+#pragma unroll
+        for (int i = 0; i < SLOTS - 1; ++i) {
+            const int64_t t2 = tile + i * (int64_t)gridDim.x;
+            if (t2 < n_tiles) prefetch_tile(p, (t2 / tiles_x) * TILE, (t2 % tiles_x) * TILE, s.tile[i]);
+            cp_async_commit();
+        }
     }
-    for (int it = 0; tile < n_tiles; tile += gridDim.x, ++it) {
-        uint16_t* cur = s.tile[it & 1];
+    for (int slot = 0; tile < n_tiles; tile += gridDim.x, slot = slot == SLOTS - 1 ? 0 : slot + 1) {
+        uint16_t* cur = s.tile[slot];
         const int64_t ty = tile / tiles_x, tx = tile % tiles_x;
         if (async) {
-            const int64_t next = tile + gridDim.x;
-            if (next < n_tiles) prefetch_tile(p, (next / tiles_x) * TILE, (next % tiles_x) * TILE, s.tile[(it + 1) & 1]);
-            cp_async_commit();    // one group per iteration (possibly empty)
-            cp_async_wait_prev(); // this thread's copies of the current tile have landed
+            const int64_t ahead = tile + (SLOTS - 1) * (int64_t)gridDim.x;
+            const int fill = slot == 0 ? SLOTS - 1 : slot - 1;  // the slot of tile it - 1
+            if (ahead < n_tiles) prefetch_tile(p, (ahead / tiles_x) * TILE, (ahead % tiles_x) * TILE, s.tile[fill]);
+            cp_async_commit();                 // one group per iteration (possibly empty)
+            cp_async_wait<SLOTS - 1>();        // this thread's copies of the current tile have landed
         } else {
             load_tile(p, ty * TILE, tx * TILE, cur, true);
         }
         __syncthreads();
         encode_tile<NVR, NVC>(p, s, cur, ty, tx);
-        __syncthreads();  // staging buffers and `cur` are free for the next tile
+        __syncthreads();  // the scale staging and `cur` are free again
     }
 }
 
@@ -762,14 +759,14 @@ int quant_sm_count() {
     return cached[dev];
 }
 
-// CTAs of the encoder: two tiles per CTA, so that the second tile's load
-// overlaps the first one's encoding.  (Measured against one tile per CTA and
-// against one CTA per resident slot looping over all tiles: two per CTA was
-// as fast as the former on the SR + H32 gradient and as fast as the latter on
-// the latency-bound weight and activation producers.)
-unsigned encoder_grid(int64_t n_tiles) { return (unsigned)((n_tiles + 1) / 2); }
+// CTAs of the encoder: one per resident slot (two per SM), each looping over
+// its tiles through the ring.
+unsigned encoder_grid(int64_t n_tiles) {
+    const int64_t slots = 2 * (int64_t)quant_sm_count();
+    return (unsigned)(n_tiles < slots ? n_tiles : slots);
+}
 
-// The encoder's shared memory (about 90 KB) is above the 48 KB default, so
+// The encoder's shared memory (about 110 KB) is above the 48 KB default, so
 // each instantiation's limit is raised once per device, under a lock.
 template <bool NVR, bool NVC>
 int launch_encoder(const QuantParams& p, cudaStream_t stream) {
