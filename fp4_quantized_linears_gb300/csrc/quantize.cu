@@ -15,10 +15,11 @@
 // NVFP4 first runs a tile-amax pre-pass (the tensor-wide / strip-wide maximum
 // that the outer factors need), so its algorithmic traffic is two reads.
 //
-// Memory behaviour: persistent CTAs, two per SM, each with a ring of three
-// tile slots filled by 16-byte cp.async copies two tiles ahead of the one
-// being encoded (about 128 KB in flight per SM); per-thread 32-value
-// segments for both orientations read from shared memory; codes stored from
+// Memory behaviour: persistent CTAs, three per SM (80 registers, 72 KB of
+// shared memory each), each with two tile slots: the next tile's 16-byte
+// cp.async copies land while one is encoded (about 96 KB in flight per SM);
+// per-thread 32-value segments for both orientations read from shared memory
+// (unpadded tiles, 16-byte chunks XOR-swizzled by row); codes stored from
 // registers (row view: the four 16-byte pieces of a row's 64 bytes from
 // adjacent lanes; column view: 16-byte pieces whose sector halves come from
 // neighbouring warps and merge in L2); scale atoms staged in shared memory and
@@ -39,14 +40,21 @@ __device__ unsigned int g_status_quant;
 namespace {
 
 constexpr int TILE = 128;
-constexpr int PAD = 8;               // bf16 elements of padding per smem row
-constexpr int LDS = TILE + PAD;      // smem row stride (elements)
 constexpr int THREADS = 256;
+constexpr int CTAS_PER_SM = 3;
 
-constexpr int SLOTS = 3;             // tile ring: the tile being encoded and the next two landing
+constexpr int SLOTS = 2;             // tile ring: the tile being encoded and the next one landing
+
+// Shared tiles are unpadded (256-byte rows) with the 16-byte chunks of row r
+// XOR-ed by r & 7: element (r, c) sits at r * 128 + ((c / 8) ^ (r & 7)) * 8 +
+// c % 8.  Every access pattern of the kernels then touches each bank once
+// per phase: the 16-byte copies and loads of a row's chunks, the 16-byte
+// loads of one chunk index over 8 consecutive rows (row segments), and the
+// 32-bit loads of 32 consecutive column pairs of one row (column view).
+FP4_DEV int tile_off(int r, int c) { return r * TILE + ((((c >> 3) ^ r) & 7) | ((c >> 3) & ~7)) * 8 + (c & 7); }
 
 struct SmemQ {
-    uint16_t tile[SLOTS][TILE * LDS];  // 3 x 34,816 B
+    uint16_t tile[SLOTS][TILE * TILE];  // 2 x 32 KB
     uint8_t row_sc[1024];            // staged scale atoms (1 MX / 2 NV)
     uint8_t col_sc[1024];
     int tile_e[16];                  // 2D32: per 32x32 tile exponent
@@ -162,7 +170,7 @@ FP4_DEV void hadamard16x2_nosign(float* v) {
     scale_all(v, 0.25f);
 }
 
-// Load the 128x128 tile at (r0, c0) into shared memory (row stride LDS),
+// Load the 128x128 tile at (r0, c0) into shared memory (tile_off layout),
 // applying the pre-op; with write_tap the pre-op results are also stored.
 FP4_DEV void load_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* tile, bool write_tap) {
     const int t = threadIdx.x;
@@ -177,7 +185,7 @@ FP4_DEV void load_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* t
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int q = t + i * THREADS;
-            *reinterpret_cast<uint4*>(&tile[(q >> 4) * LDS + (q & 15) * 8]) = d[i];
+            *reinterpret_cast<uint4*>(&tile[tile_off(q >> 4, (q & 15) * 8)]) = d[i];
         }
         return;
     }
@@ -220,8 +228,8 @@ FP4_DEV void load_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* t
                 *reinterpret_cast<uint4*>(p.tap + tok * p.C + c0 + 8 * g) = lo;
                 *reinterpret_cast<uint4*>(p.tap + tok * p.C + c0 + 64 + 8 * g) = hi;
             }
-            *reinterpret_cast<uint4*>(&tile[rr * LDS + 8 * g]) = lo;
-            *reinterpret_cast<uint4*>(&tile[rr * LDS + 64 + 8 * g]) = hi;
+            *reinterpret_cast<uint4*>(&tile[tile_off(rr, 8 * g)]) = lo;
+            *reinterpret_cast<uint4*>(&tile[tile_off(rr, 64 + 8 * g)]) = hi;
         }
         return;
     }
@@ -267,7 +275,7 @@ FP4_DEV void load_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* t
             d = make_uint4(os[0], os[1], os[2], os[3]);
             if (write_tap && p.tap) *reinterpret_cast<uint4*>(p.tap + gr * p.C + gc) = d;
         }
-        *reinterpret_cast<uint4*>(&tile[rr * LDS + cc]) = d;
+        *reinterpret_cast<uint4*>(&tile[tile_off(rr, cc)]) = d;
     }
 }
 
@@ -298,12 +306,6 @@ FP4_DEV void segment_scale(uint32_t am0, uint32_t am1, float senc, uint8_t* sc_b
         sc_base[atom_off(lr, 2 * lj)] = (uint8_t)nv_block_scale(__uint_as_float(am0), senc, m0);
         sc_base[atom_off(lr, 2 * lj + 1)] = (uint8_t)nv_block_scale(__uint_as_float(am1), senc, m1);
     }
-}
-
-// Unpack the low (h = 0) or high (h = 1) bf16 lanes of 32 words into fp32.
-FP4_DEV void unpack_lane(const uint32_t* w, int h, float* v) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
 }
 
 // Encode the 128x128 tile (ty, tx), already in shared memory at `tbuf`, into
@@ -365,10 +367,9 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
     // 16-byte shared loads of this thread's row segment k (steps 2 and 3)
     auto load_segment = [&](int k, uint32_t* w) {
         const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
-        const uint16_t* src = &tbuf[r * LDS + j * 32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint4 d = *reinterpret_cast<const uint4*>(src + 8 * q);
+            const uint4 d = *reinterpret_cast<const uint4*>(&tbuf[tile_off(r, 32 * j + 8 * q)]);
             w[4 * q] = d.x; w[4 * q + 1] = d.y; w[4 * q + 2] = d.z; w[4 * q + 3] = d.w;
         }
     };
@@ -473,39 +474,36 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
         }
     }
 
-    // 4. column-facing view: thread = (column pair cp, row block j); the pair
-    //    (2 cp, 2 cp + 1) is read as 32 bf16x2 words down the tile, and each
-    //    column is one 32-value segment of its stored row (blocks along the rows)
+    // 4. column-facing view: thread = (column pair cp, row block j); each
+    //    column of the pair (2 cp, then 2 cp + 1) is one 32-value segment of
+    //    its stored row (blocks along the rows), read down the tile with
+    //    16-bit loads (one column at a time keeps the register count low)
     if (do_col) {
         const bool had = (p.flags & FP4_FLAG_HADAMARD_COL) != 0;  // H32 (MXFP4)
         const int cp = t & 63, j = t >> 6;
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tbuf[(j * 32 + i) * LDS + 2 * cp]);
-        if (had || h16) {
-            // the sign of position i (mod 16) applies to both columns of the pair
-#pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] ^= ((p.sign_mask >> (i & 15)) & 1u) * 0x80008000u;
-        }
-        uint32_t a_lo0 = 0, a_hi0 = 0, a_lo1 = 0, a_hi1 = 0;  // NV: [h][block]
-        if (!had && !h16 && !w2d) {
-            if (!NVC) {
-                const uint32_t a2 = amax_words<32>(w);
-                a_lo0 = lane_lo_f32bits(a2);
-                a_hi0 = lane_hi_f32bits(a2);
-            } else {
-                const uint32_t b0 = amax_words<16>(w), b1 = amax_words<16>(w + 16);
-                a_lo0 = lane_lo_f32bits(b0);
-                a_hi0 = lane_hi_f32bits(b0);
-                a_lo1 = lane_lo_f32bits(b1);
-                a_hi1 = lane_hi_f32bits(b1);
-            }
-        }
+        // the fixed sign of position i (mod 16) as the bf16 sign bit (a mask
+        // of zero flips nothing and takes the loop without the flips)
+        const uint32_t sgn = (had || h16) ? p.sign_mask : 0u;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
             const int c = 2 * cp + h;
+            // column c of rows j * 32 + i: the swizzle depends on i & 7 only,
+            // so eight element offsets serve all 32 loads
+            const uint16_t* col = tbuf + j * 32 * TILE;
+            int off[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) off[k] = tile_off(k, c) - k * TILE;
             float v[32];
-            unpack_lane(w, h, v);
+            if (sgn) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const uint32_t b = col[i * TILE + off[i & 7]] ^ ((sgn << (15 - (i & 15))) & 0x8000u);
+                    v[i] = __uint_as_float(b << 16);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float((uint32_t)col[i * TILE + off[i & 7]] << 16);
+            }
             float m0, m1;
             if (w2d) {
                 if (!NVC) {
@@ -528,9 +526,10 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                     segment_scale<true>(amax_bits16(v), amax_bits16(v + 16), senc_col, s.col_sc, c, j, m0, m1);
                 else
                     segment_scale<false>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
+            } else if (!NVC) {
+                segment_scale<false>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
             } else {
-                segment_scale<NVC>(h ? a_hi0 : a_lo0, h ? a_hi1 : a_lo1, senc_col, s.col_sc, c, j, m0, m1,
-                                   NVC ? s.mtab[1] : nullptr);
+                segment_scale<true>(amax_bits16(v), amax_bits16(v + 16), senc_col, s.col_sc, c, j, m0, m1, s.mtab[1]);
             }
             *reinterpret_cast<uint4*>(p.col_codes + (c0 + c) * (p.R >> 1) + (r0 >> 1) + j * 16) = pack_rn32(v, m0, m1);
         }
@@ -569,24 +568,24 @@ FP4_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memo
 template <int N>
 FP4_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Start loading the 128x128 tile at (r0, c0) into `tile` (row stride LDS).
+// Start loading the 128x128 tile at (r0, c0) into `tile` (tile_off layout).
 FP4_DEV void prefetch_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_t* tile) {
     const int t = threadIdx.x;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int q = t + i * THREADS;
-        cp_async16(&tile[(q >> 4) * LDS + (q & 15) * 8], p.x + (r0 + (q >> 4)) * p.ld + c0 + (q & 15) * 8);
+        cp_async16(&tile[tile_off(q >> 4, (q & 15) * 8)], p.x + (r0 + (q >> 4)) * p.ld + c0 + (q & 15) * 8);
     }
 }
 
 // Each CTA walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... (row-strip-major
-// order) through a ring of three tile slots: while one tile is encoded the
-// next two are in flight (one commit group per tile, possibly empty), so the
-// load latency hides behind two tiles' encoding.  Slot (it + 2) % 3 is
-// refilled only after the barrier that ends tile it - 1, its last reader.
+// order) through a ring of SLOTS tile slots: while one tile is encoded the
+// next SLOTS - 1 are in flight (one commit group per tile, possibly empty).
+// The slot of tile it + SLOTS - 1 is refilled only after the barrier that
+// ends tile it - 1, its last reader.
 // With an RMSNorm pre-op the tile is loaded (and transformed) synchronously.
 template <bool NVR, bool NVC>
-__global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(const __grid_constant__ QuantParams p) {
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM) quantize_tile_kernel(const __grid_constant__ QuantParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
     const int64_t tiles_x = p.C / TILE, n_tiles = tiles_x * (p.R / TILE);
@@ -606,7 +605,7 @@ __global__ void __launch_bounds__(THREADS, 2) quantize_tile_kernel(const __grid_
         const int64_t ty = tile / tiles_x, tx = tile % tiles_x;
         if (async) {
             const int64_t ahead = tile + (SLOTS - 1) * (int64_t)gridDim.x;
-            const int fill = slot == 0 ? SLOTS - 1 : slot - 1;  // the slot of tile it - 1
+            const int fill = slot == 0 ? SLOTS - 1 : slot - 1;  // the slot of tile it - 1 (ring order)
             if (ahead < n_tiles) prefetch_tile(p, (ahead / tiles_x) * TILE, (ahead % tiles_x) * TILE, s.tile[fill]);
             cp_async_commit();                 // one group per iteration (possibly empty)
             cp_async_wait<SLOTS - 1>();        // this thread's copies of the current tile have landed
@@ -644,7 +643,7 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(const __grid_constant_
     for (int i = 0; i < 8; ++i) {
         int q = t + i * THREADS;
         int rr = q >> 4, cc = (q & 15) * 8;
-        uint4 d = staged ? *reinterpret_cast<const uint4*>(&tile[rr * LDS + cc])
+        uint4 d = staged ? *reinterpret_cast<const uint4*>(&tile[tile_off(rr, cc)])
                          : *reinterpret_cast<const uint4*>(p.x + (r0 + rr) * p.ld + c0 + cc);
         uint32_t w[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
@@ -661,7 +660,7 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(const __grid_constant_
             float v[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(jb * 16 + i) * LDS + 2 * cp]);
+                uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[tile_off(jb * 16 + i, 2 * cp)]);
                 w ^= ((p.sign_mask >> i) & 1u) * 0x80008000u;
                 v[i] = bf16_lo(w);
                 v[16 + i] = bf16_hi(w);
@@ -759,14 +758,16 @@ int quant_sm_count() {
     return cached[dev];
 }
 
-// CTAs of the encoder: one per resident slot (two per SM), each looping over
-// its tiles through the ring.
+// CTAs of the encoder: one per resident slot (three per SM), each looping
+// over its tiles through the ring.  (Measured: two CTAs of 128 registers
+// with a three-slot ring, or two tiles per CTA, were slower: the encoders
+// are latency-bound at four warps per scheduler.)
 unsigned encoder_grid(int64_t n_tiles) {
-    const int64_t slots = 2 * (int64_t)quant_sm_count();
+    const int64_t slots = CTAS_PER_SM * (int64_t)quant_sm_count();
     return (unsigned)(n_tiles < slots ? n_tiles : slots);
 }
 
-// The encoder's shared memory (about 110 KB) is above the 48 KB default, so
+// The encoder's shared memory (about 72 KB) is above the 48 KB default, so
 // each instantiation's limit is raised once per device, under a lock.
 template <bool NVR, bool NVC>
 int launch_encoder(const QuantParams& p, cudaStream_t stream) {
@@ -810,7 +811,7 @@ int launch_quantize(const QuantParams& p, cudaStream_t stream) {
         if (cudaMemsetAsync(p.amax_ws, 0, slots * 4, stream) != cudaSuccess) return FP4_ERR_CUDA;
         const bool col_h16 = (p.flags & FP4_FLAG_HADAMARD16_COL) && do_col && p.col_route != FP4_ROUTE_MXFP4;
         if (p.pre != PRE_NONE || col_h16) {
-            const size_t amax_smem = sizeof(uint16_t) * TILE * LDS;
+            const size_t amax_smem = sizeof(uint16_t) * TILE * TILE;
             dim3 grid((unsigned)(p.C / TILE), (unsigned)(p.R / TILE));
             nv_amax_kernel<<<grid, THREADS, amax_smem, stream>>>(p);
         } else {
