@@ -60,7 +60,6 @@ struct SmemQ {
     int tile_e[16];                  // 2D32: per 32x32 tile exponent
     float tile_m[64];                // 2D16: per 16x16 tile multiplier
     uint32_t tile_d[64];             // 2D16: per 16x16 tile E4M3 byte
-    uint32_t seg_amax[TILE * 8];     // 2D: |max| bits of each 16-value row piece
     float mtab[2][128];              // NVFP4: S_enc / E4M3(d) of the row / column view's factor
     uint32_t red[THREADS / 32];
 };
@@ -68,11 +67,12 @@ struct SmemQ {
 
 // Byte offset of local block j (0..nb-1) of local row r in staged atoms.
 // Row segments: work item idx (0 .. 511) is 32-value segment j of local row
-// r, numbered so that the 8 lanes of each 16-byte shared-load phase read 8
-// consecutive rows at the same j (the padded row stride then spreads them
-// over all 32 banks; four segments of one row would pair up 128 bytes apart).
-FP4_DEV int seg_row(int idx) { return (idx & 7) + 8 * (idx >> 5); }
-FP4_DEV int seg_j(int idx) { return (idx >> 3) & 3; }
+// r, numbered so that each warp holds 32 consecutive rows at one j: a 32x32
+// block of the tile is one warp's segments (2D weight maxima by shuffles),
+// and the 8 lanes of each 16-byte shared-load phase read 8 consecutive rows
+// at one chunk index, which the tile swizzle spreads over all 32 banks.
+FP4_DEV int seg_row(int idx) { return (idx & 31) + 32 * (idx >> 7); }
+FP4_DEV int seg_j(int idx) { return (idx >> 5) & 3; }
 
 FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
 
@@ -374,58 +374,10 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
         }
     };
 
-    // 2. shared 2D weight scales: the maxima of the 16-value pieces of every
-    //    row (16-byte shared loads), then one reduction per tile
-    if (w2d) {
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
-            const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
-            uint32_t w[16];
-            load_segment(k, w);
-            const uint32_t a0 = amax_words<8>(w), a1 = amax_words<8>(w + 8);
-            s.seg_amax[r * 8 + 2 * j] = max(lane_lo_f32bits(a0), lane_hi_f32bits(a0));
-            s.seg_amax[r * 8 + 2 * j + 1] = max(lane_lo_f32bits(a1), lane_hi_f32bits(a1));
-        }
-        __syncthreads();
-        if (!NVR || !NVC) {
-            // 16 tiles of 32x32: 16 threads per tile, two rows each
-            const int tile = t >> 4, part = t & 15, tr = tile >> 2, tc = tile & 3;
-            uint32_t m = 0;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int r = tr * 32 + part * 2 + i;
-                m = max(m, max(s.seg_amax[r * 8 + 2 * tc], s.seg_amax[r * 8 + 2 * tc + 1]));
-            }
-#pragma unroll
-            for (int o = 8; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-            if (part == 0) {
-                check_finite(m);
-                int e = e8m0_exponent_up(m);
-                // adaptive rule: finer exponent when a_T * 2^-e < fl32(5.22)
-                if (__fmul_rn(__uint_as_float(m), exp2_neg(e)) < 5.22f && e > -127) e -= 1;
-                s.tile_e[tile] = e;
-            }
-        }
-        if (NVR || NVC) {
-            // 64 tiles of 16x16: 4 threads per tile, four rows each
-            const int tile = t >> 2, part = t & 3, tr = tile >> 3, tc = tile & 7;
-            uint32_t m = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) m = max(m, s.seg_amax[(tr * 16 + part * 4 + i) * 8 + tc]);
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            if (part == 0) {
-                check_finite(m);
-                float mm;
-                s.tile_d[tile] = nv_block_scale_bf16(__uint_as_float(m), senc_w, s.mtab[NVR ? 0 : 1], mm);
-                s.tile_m[tile] = mm;
-            }
-        }
-        __syncthreads();
-    }
-
-    // 3. row-facing view: segment (r, j) = 32 values of local row r starting at 32 j
-    if (do_row) {
+    // 2-3. row-facing view: segment (r, j) = 32 values of local row r
+    //      starting at 32 j; 2D weights first take their shared tile scales
+    //      from the same registers
+    {
         const bool sr = (p.flags & FP4_FLAG_SR_ROW) != 0;
         auto row_segment = [&](int k, const uint32_t* w) {
             const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
@@ -466,11 +418,61 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
             }
             *reinterpret_cast<uint4*>(p.row_codes + (r0 + r) * (p.C >> 1) + (c0 >> 1) + j * 16) = packed;
         };
+        if (w2d) {
+            // The warp's segments are the 32x32 block (rows 32 (r / 32) ..,
+            // columns 32 j ..): its maximum by shuffles over the 32 lanes; a
+            // 16x16 block is one half-warp's 16-value pieces.  The scales go
+            // to shared memory for the column view (after the barrier below)
+            // and for this warp's own row segments (after __syncwarp).
+            const int lane = t & 31;
 #pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
-            uint32_t w[16];
-            load_segment(k, w);
-            row_segment(k, w);
+            for (int k = 0; k < 2; ++k) {
+                const int idx = t + k * THREADS, r = seg_row(idx), j = seg_j(idx);
+                uint32_t w[16];
+                load_segment(k, w);
+                const uint32_t a0 = amax_words<8>(w), a1 = amax_words<8>(w + 8);
+                uint32_t ma = max(lane_lo_f32bits(a0), lane_hi_f32bits(a0));
+                uint32_t mb = max(lane_lo_f32bits(a1), lane_hi_f32bits(a1));
+                if (!NVR || !NVC) {
+                    uint32_t m = max(ma, mb);
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                    if (lane == 0) {
+                        check_finite(m);
+                        int e = e8m0_exponent_up(m);
+                        // adaptive rule: finer exponent when a_T * 2^-e < fl32(5.22)
+                        if (__fmul_rn(__uint_as_float(m), exp2_neg(e)) < 5.22f && e > -127) e -= 1;
+                        s.tile_e[(r >> 5) * 4 + j] = e;
+                    }
+                }
+                if (NVR || NVC) {
+#pragma unroll
+                    for (int o = 8; o; o >>= 1) {
+                        ma = max(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, o));
+                        mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+                    }
+                    if ((lane & 15) == 0) {
+                        check_finite(max(ma, mb));
+                        const int tl = (r >> 4) * 8 + 2 * j;
+                        const float* mt = s.mtab[NVR ? 0 : 1];
+                        float mm;
+                        s.tile_d[tl] = nv_block_scale_bf16(__uint_as_float(ma), senc_w, mt, mm);
+                        s.tile_m[tl] = mm;
+                        s.tile_d[tl + 1] = nv_block_scale_bf16(__uint_as_float(mb), senc_w, mt, mm);
+                        s.tile_m[tl + 1] = mm;
+                    }
+                }
+                __syncwarp();
+                if (do_row) row_segment(k, w);
+            }
+            __syncthreads();  // every tile scale, for the column view
+        } else if (do_row) {
+#pragma unroll 1
+            for (int k = 0; k < 2; ++k) {
+                uint32_t w[16];
+                load_segment(k, w);
+                row_segment(k, w);
+            }
         }
     }
 
