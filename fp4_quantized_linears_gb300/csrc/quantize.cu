@@ -61,6 +61,7 @@ struct SmemQ {
     float tile_m[64];                // 2D16: per 16x16 tile multiplier
     uint32_t tile_d[64];             // 2D16: per 16x16 tile E4M3 byte
     float mtab[2][128];              // NVFP4: S_enc / E4M3(d) of the row / column view's factor
+    float signf[16];                 // the Hadamard's fixed signs as +-1 (set once per CTA)
     uint32_t red[THREADS / 32];
 };
 
@@ -126,16 +127,19 @@ FP4_DEV uint4 pack_sr32(const uint32_t* w, float m0, float m1, uint64_t g0, cons
 }
 
 // Butterfly stages of strides 1 .. H/2 on each H-value group of 32
-// registers.  Stride 1 pairs the two lanes of a register pair (v[2i],
-// v[2i + 1]) and runs scalar; every wider stride pairs whole register pairs
-// and runs on f32x2 lanes.
+// registers, after the fixed signs sg[i mod 16] (+-1) of Sec. 2.5.  Stride 1
+// pairs the two lanes of a register pair (v[2i], v[2i + 1]) and runs scalar,
+// with the signs folded in: u = s v is exact, so fl(u0 + u1) =
+// fma(s1, v1, s0 v0) and fl(u0 - u1) = fma(-s1, v1, s0 v0) give the bits of
+// flipping first (the flips then cost no integer instructions); every wider
+// stride pairs whole register pairs and runs on f32x2 lanes.
 template <int H>
-FP4_DEV void butterflies(float* v) {
+FP4_DEV void butterflies(float* v, const float* sg) {
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-        const float a = v[j], b = v[j + 1];
-        v[j] = __fadd_rn(a, b);
-        v[j + 1] = __fsub_rn(a, b);
+        const float t = __fmul_rn(v[j], sg[j & 15]), s1 = sg[(j + 1) & 15], b = v[j + 1];
+        v[j] = __fmaf_rn(s1, b, t);
+        v[j + 1] = __fmaf_rn(-s1, b, t);
     }
 #pragma unroll
     for (int h = 2; h < H; h <<= 1) {
@@ -154,19 +158,21 @@ FP4_DEV void scale_all(float* v, float s) {
     for (int i = 0; i < 32; i += 2) f32x2_mul(v[i], v[i + 1], v[i], v[i + 1], s, s);
 }
 
-// H32 butterflies on 32 registers whose fixed signs were already applied:
-// stages of stride 1, 2, 4, 8 within each 16-value half, then the cross-half
-// stage of stride 16, then the binary32 multiply by fl32(1/sqrt(32)).
-FP4_DEV void hadamard32_nosign(float* v) {
-    butterflies<32>(v);
+__device__ const float kUnitSigns[16] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f,
+                                         1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+
+// Fixed-sign H32 on 32 registers (signs sg): stages of stride 1, 2, 4, 8
+// within each 16-value half, then the cross-half stage of stride 16, then the
+// binary32 multiply by fl32(1/sqrt(32)).
+FP4_DEV void hadamard32(float* v, const float* sg) {
+    butterflies<32>(v, sg);
     scale_all(v, __uint_as_float(0x3E3504F3u));  // fl32(1 / sqrt(32))
 }
 
-// H16 butterflies on each 16-value half of 32 registers whose fixed signs
-// were already applied: stages of stride 1, 2, 4, 8, then the multiply by
-// 1/sqrt(16) = 0.25 (exact).
-FP4_DEV void hadamard16x2_nosign(float* v) {
-    butterflies<16>(v);
+// Fixed-sign H16 on each 16-value half of 32 registers (signs sg): stages
+// of stride 1, 2, 4, 8, then the multiply by 1/sqrt(16) = 0.25 (exact).
+FP4_DEV void hadamard16x2(float* v, const float* sg) {
+    butterflies<16>(v, sg);
     scale_all(v, 0.25f);
 }
 
@@ -483,9 +489,6 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
     if (do_col) {
         const bool had = (p.flags & FP4_FLAG_HADAMARD_COL) != 0;  // H32 (MXFP4)
         const int cp = t & 63, j = t >> 6;
-        // the fixed sign of position i (mod 16) as the bf16 sign bit (a mask
-        // of zero flips nothing and takes the loop without the flips)
-        const uint32_t sgn = (had || h16) ? p.sign_mask : 0u;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
             const int c = 2 * cp + h;
@@ -496,16 +499,8 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
 #pragma unroll
             for (int k = 0; k < 8; ++k) off[k] = tile_off(k, c) - k * TILE;
             float v[32];
-            if (sgn) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint32_t b = col[i * TILE + off[i & 7]] ^ ((sgn << (15 - (i & 15))) & 0x8000u);
-                    v[i] = __uint_as_float(b << 16);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float((uint32_t)col[i * TILE + off[i & 7]] << 16);
-            }
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float((uint32_t)col[i * TILE + off[i & 7]] << 16);
             float m0, m1;
             if (w2d) {
                 if (!NVC) {
@@ -520,10 +515,10 @@ FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, i
                     s.col_sc[atom_off(c, 2 * j + 1)] = (uint8_t)s.tile_d[tl + 8];
                 }
             } else if (had) {
-                hadamard32_nosign(v);
+                hadamard32(v, s.signf);
                 segment_scale<NVC>(amax_bits32(v), 0, senc_col, s.col_sc, c, j, m0, m1);
             } else if (h16) {
-                hadamard16x2_nosign(v);
+                hadamard16x2(v, s.signf);
                 if (NVC)
                     segment_scale<true>(amax_bits16(v), amax_bits16(v + 16), senc_col, s.col_sc, c, j, m0, m1);
                 else
@@ -594,6 +589,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) quantize_tile_kernel(con
     const bool async = p.pre == PRE_NONE;
     int64_t tile = blockIdx.x;
     if (tile >= n_tiles) return;
+    // the Hadamard's fixed signs (read after the first tile's barrier)
+    if (threadIdx.x < 16) s.signf[threadIdx.x] = ((p.sign_mask >> threadIdx.x) & 1u) ? -1.0f : 1.0f;
     if (async) {
 #pragma unroll
         for (int i = 0; i < SLOTS - 1; ++i) {
@@ -667,7 +664,7 @@ __global__ void __launch_bounds__(THREADS) nv_amax_kernel(const __grid_constant_
                 v[i] = bf16_lo(w);
                 v[16 + i] = bf16_hi(w);
             }
-            hadamard16x2_nosign(v);
+            hadamard16x2(v, kUnitSigns);  // the signs are already applied to the words
             mc = max(mc, max(amax_bits16(v), amax_bits16(v + 16)));
         }
     }
