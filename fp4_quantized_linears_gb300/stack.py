@@ -233,6 +233,26 @@ class FP4LinearStack:
         self.step_index += 1
         return out
 
+    def capture_steps(self, x: torch.Tensor, dy: torch.Tensor, steps: int, sr_seed: int = 1):
+        """Record `steps` consecutive training steps (each with its own step
+        index, hence its own stochastic-rounding draws) into one CUDA graph
+        and return it; replaying it runs exactly those launches with no host
+        work between them.  Every buffer the steps touch is allocated
+        beforehand, so nothing allocates while recording; run one eager step
+        first, so that the library's one-time per-device setup is done."""
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        timing, self.time_standin = self.time_standin, False
+        try:
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(steps):
+                    self.step(x, dy, sr_seed)
+        finally:
+            self.time_standin = timing
+        torch.cuda.current_stream().wait_stream(side)
+        return graph
+
     def standin_ms(self) -> float:
         """Device milliseconds of the attention stand-in's copies recorded
         since the last call (time_standin must be set); synchronises."""
