@@ -687,6 +687,8 @@ def run_stack_leg(args, out: dict, peaks=None) -> dict:
     # the graph too and are taken out as above)
     graph_note = "cuda graph of the timed steps, replayed"
     try:
+        if args.stack_eager:
+            raise RuntimeError("--stack-eager")
         graph = st.capture_steps(x5, dy5, steps, sr_seed=5)
         graph.replay()
         torch.cuda.synchronize()
@@ -697,7 +699,8 @@ def run_stack_leg(args, out: dict, peaks=None) -> dict:
         ms_all = e0.elapsed_time(e1) / steps
         del graph
     except RuntimeError as exc:  # capture refused: report the eager launches
-        graph_note = f"eager launches (graph capture failed: {str(exc).splitlines()[0][:120]})"
+        graph_note = ("eager launches" if args.stack_eager else
+                      f"eager launches (graph capture failed: {str(exc).splitlines()[0][:120]})")
         ms_all = ms_eager_all
     if F.fp4_status() != F.FP4_OK:
         raise RuntimeError("device status set in the stack leg")
@@ -853,6 +856,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--stack-eager", action="store_true",
+                    help="stack leg: time the eager launches only (no CUDA graph of the timed steps)")
     ap.add_argument("--no-legs", action="store_true", help="only the main workload")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-block stack leg")
     ap.add_argument("--stack-blocks", type=int, default=32, help="blocks of the stack leg (profiling-sized runs)")
