@@ -20,9 +20,10 @@
 // cp.async copies land while one is encoded (about 96 KB in flight per SM);
 // per-thread 32-value segments for both orientations read from shared memory
 // (unpadded tiles, 16-byte chunks XOR-swizzled by row); codes stored from
-// registers (row view: the four 16-byte pieces of a row's 64 bytes from
-// adjacent lanes; column view: 16-byte pieces whose sector halves come from
-// neighbouring warps and merge in L2); scale atoms staged in shared memory and
+// registers as 16-byte pieces whose sector halves come from neighbouring
+// warps and merge in L2 (row view: the four pieces of a row's 64 bytes from
+// the four warps of its block indices; column view likewise down the stored
+// rows); scale atoms staged in shared memory and
 // written with coalesced 16-byte stores (each tile's scale bytes form whole
 // 512-byte atoms).
 #include <cuda_runtime.h>
