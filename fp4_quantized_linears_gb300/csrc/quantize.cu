@@ -15,9 +15,10 @@
 // NVFP4 first runs a tile-amax pre-pass (the tensor-wide / strip-wide maximum
 // that the outer factors need), so its algorithmic traffic is two reads.
 //
-// Memory behaviour: persistent CTAs, three per SM (80 registers, 72 KB of
-// shared memory each), each with two tile slots: the next tile's 16-byte
-// cp.async copies land while one is encoded (about 96 KB in flight per SM);
+// Memory behaviour: persistent CTAs, four per SM (64 registers, one tile slot
+// of 16-byte cp.async copies each: the other CTAs' encoding hides a CTA's
+// load) or, for the MXFP4 row view with stochastic rounding, three per SM (80
+// registers, two slots: the next tile lands while one is encoded);
 // per-thread 32-value segments for both orientations read from shared memory
 // (unpadded tiles, 16-byte chunks XOR-swizzled by row); codes stored from
 // registers as 16-byte pieces whose sector halves come from neighbouring
@@ -42,9 +43,14 @@ namespace {
 
 constexpr int TILE = 128;
 constexpr int THREADS = 256;
-constexpr int CTAS_PER_SM = 3;
 
-constexpr int SLOTS = 2;             // tile ring: the tile being encoded and the next one landing
+// CTAs per SM of an encoder launch: three at 80 registers with two tile
+// slots each (the tile being encoded and the next one landing), or four at
+// 64 registers with one slot (the other CTAs' work hides each one's load).
+// Four are 1-6 % faster on every route but the MXFP4 row view with
+// stochastic rounding, which is 2 % slower with four and takes three.
+template <int CTAS>
+constexpr int slots_of() { return CTAS == 4 ? 1 : 2; }
 
 // Shared tiles are unpadded (256-byte rows) with the 16-byte chunks of row r
 // XOR-ed by r & 7: element (r, c) sits at r * 128 + ((c / 8) ^ (r & 7)) * 8 +
@@ -54,8 +60,9 @@ constexpr int SLOTS = 2;             // tile ring: the tile being encoded and th
 // 32-bit loads of 32 consecutive column pairs of one row (column view).
 FP4_DEV int tile_off(int r, int c) { return r * TILE + ((((c >> 3) ^ r) & 7) | ((c >> 3) & ~7)) * 8 + (c & 7); }
 
+template <int SLOTS>
 struct SmemQ {
-    uint16_t tile[SLOTS][TILE * TILE];  // 2 x 32 KB
+    uint16_t tile[SLOTS][TILE * TILE];  // SLOTS x 32 KB
     uint8_t row_sc[1024];            // staged scale atoms (1 MX / 2 NV)
     uint8_t col_sc[1024];
     int tile_e[16];                  // 2D32: per 32x32 tile exponent
@@ -319,8 +326,8 @@ FP4_DEV void segment_scale(uint32_t am0, uint32_t am1, float senc, uint8_t* sc_b
 // both views: steps 2-5 below.  NVR / NVC: the row / column view is NVFP4
 // (else MXFP4); the two differ in the operand-wise hybrid producer.  Called
 // by all threads of the CTA with the tile visible to every thread.
-template <bool NVR, bool NVC>
-FP4_DEV void encode_tile(const QuantParams& p, SmemQ& s, const uint16_t* tbuf, int64_t ty, int64_t tx) {
+template <bool NVR, bool NVC, class SmemT>
+FP4_DEV void encode_tile(const QuantParams& p, SmemT& s, const uint16_t* tbuf, int64_t ty, int64_t tx) {
     const int t = threadIdx.x;
     const int64_t r0 = ty * TILE, c0 = tx * TILE;
     const bool w2d = (p.flags & FP4_FLAG_WEIGHT_2D) != 0;
@@ -582,10 +589,11 @@ FP4_DEV void prefetch_tile(const QuantParams& p, int64_t r0, int64_t c0, uint16_
 // The slot of tile it + SLOTS - 1 is refilled only after the barrier that
 // ends tile it - 1, its last reader.
 // With an RMSNorm pre-op the tile is loaded (and transformed) synchronously.
-template <bool NVR, bool NVC>
-__global__ void __launch_bounds__(THREADS, CTAS_PER_SM) quantize_tile_kernel(const __grid_constant__ QuantParams p) {
+template <bool NVR, bool NVC, int CTAS>
+__global__ void __launch_bounds__(THREADS, CTAS) quantize_tile_kernel(const __grid_constant__ QuantParams p) {
+    constexpr int SLOTS = slots_of<CTAS>();
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    SmemQ& s = *reinterpret_cast<SmemQ*>(smem_raw);
+    SmemQ<SLOTS>& s = *reinterpret_cast<SmemQ<SLOTS>*>(smem_raw);
     const int64_t tiles_x = p.C / TILE, n_tiles = tiles_x * (p.R / TILE);
     const bool async = p.pre == PRE_NONE;
     int64_t tile = blockIdx.x;
@@ -758,20 +766,21 @@ int quant_sm_count() {
     return cached[dev];
 }
 
-// CTAs of the encoder: one per resident slot (three per SM), each looping
-// over its tiles through the ring.  (Measured: two CTAs of 128 registers
+// CTAs of the encoder: one per resident slot (CTAS per SM), each looping
+// over its tiles through its ring.  (Measured: two CTAs of 128 registers
 // with a three-slot ring, or two tiles per CTA, were slower: the encoders
 // are latency-bound at four warps per scheduler.)
-unsigned encoder_grid(int64_t n_tiles) {
-    const int64_t slots = CTAS_PER_SM * (int64_t)quant_sm_count();
+unsigned encoder_grid(int64_t n_tiles, int ctas) {
+    const int64_t slots = ctas * (int64_t)quant_sm_count();
     return (unsigned)(n_tiles < slots ? n_tiles : slots);
 }
 
-// The encoder's shared memory (about 72 KB) is above the 48 KB default, so
-// each instantiation's limit is raised once per device, under a lock.
-template <bool NVR, bool NVC>
-int launch_encoder(const QuantParams& p, cudaStream_t stream) {
-    const size_t smem = sizeof(SmemQ);
+// The encoder's shared memory (about 72 or 40 KB) is above the 48 KB default
+// (or close to it), so each instantiation's limit is raised once per device,
+// under a lock.
+template <bool NVR, bool NVC, int CTAS>
+int launch_encoder_n(const QuantParams& p, cudaStream_t stream) {
+    const size_t smem = sizeof(SmemQ<slots_of<CTAS>()>);
     static std::mutex mu;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -779,17 +788,24 @@ int launch_encoder(const QuantParams& p, cudaStream_t stream) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_done[dev]) {
-            if (cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess ||
-                cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     100) != cudaSuccess)
+            if (cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC, CTAS>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+                cudaFuncSetAttribute(quantize_tile_kernel<NVR, NVC, CTAS>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
                 return FP4_ERR_CUDA;
             attr_done[dev] = true;
         }
     }
     const int64_t n_tiles = (p.C / TILE) * (p.R / TILE);
-    quantize_tile_kernel<NVR, NVC><<<encoder_grid(n_tiles), THREADS, smem, stream>>>(p);
+    quantize_tile_kernel<NVR, NVC, CTAS><<<encoder_grid(n_tiles, CTAS), THREADS, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+template <bool NVR, bool NVC>
+int launch_encoder(const QuantParams& p, cudaStream_t stream) {
+    if constexpr (!NVR) {
+        if ((p.views & FP4_VIEW_ROW) && (p.flags & FP4_FLAG_SR_ROW)) return launch_encoder_n<NVR, NVC, 3>(p, stream);
+    }
+    return launch_encoder_n<NVR, NVC, 4>(p, stream);
 }
 
 }  // namespace
