@@ -527,10 +527,6 @@ FP4_DEV uint32_t bf16x2_rn(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
-FP4_DEV void store_words16(uint16_t* dst, const uint32_t* w) {
-#pragma unroll
-    for (int i = 0; i < 16; i += 4) *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
-}
 
 FP4_DEV void store_bf16x32(uint16_t* dst, const float* v) {
 #pragma unroll
@@ -1293,7 +1289,11 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 box_free();
                 put_row(p3);
                 store_box(&tmY);
-                if (p.tap0) store_words16(p.tap0 + m * p.f + n, hp);
+                if (p.tap0) {  // the h tap through the box as well (tmC maps it)
+                    box_free();
+                    put_row(hp);
+                    store_box(&tmC);
+                }
                 if (p.amax_ws) {
                     // the tap's maxima for the NVFP4 encode that follows: the
                     // tile's 128-row strip, its 128-column strip, the tensor
@@ -1367,7 +1367,25 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 // row da1, row da3, column da1, column da3; double-buffered by tile
                 uint8_t* atoms = staging + EW * C::FWD_BOX + (acc_phase & 1) * 2048;
                 const int64_t f2 = 2 * p.f;
-                if (p.tap0) store_words16(p.tap0 + m * p.f + n, dp);
+                // The taps leave through this warp's 2 KB box (its 32 x 32
+                // block: 32 rows x 64 bytes, 64B swizzle) by TMA tensor stores
+                // (tmY maps dh, tmX [da1 | da3]); direct 16-byte stores from
+                // the lanes were ~10 % slower on the NVFP4 route.
+                auto tap_store = [&](const uint32_t* w, const CUtensorMap* map, int x) {
+                    if (lane == 0) bulk_wait_read<0>();  // the box's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(box + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(map, box, x, (int)(m0 + q * 32));
+                        bulk_commit();
+                    }
+                };
+                if (p.tap0) tap_store(dp, &tmY, (int)n);
                 // da1 = bf16(dh * a3 * SiLU'(a1)), da3 = bf16(dh * SiLU(a1)), as bf16x2 words
                 uint32_t q1[16], q3[16];
                 {
@@ -1415,8 +1433,8 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 // the slot's values are consumed: the next tile's segments may land
                 prefetch_a13(u + n_clusters);
                 if (p.tap1) {
-                    store_words16(p.tap1 + m * f2 + n, q1);
-                    store_words16(p.tap1 + m * f2 + p.f + n, q3);
+                    tap_store(q1, &tmX, (int)n);
+                    tap_store(q3, &tmX, (int)(p.f + n));
                 }
                 if (p.amax_ws) {
                     // maxima of the [da1 | da3] tap: the tile's row strip
@@ -1444,6 +1462,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
 #pragma unroll 1
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t* src = which ? q3 : q1;
+                        if (lane == 0) bulk_wait_read<0>();  // a tap store may still read the box
                         __syncwarp();  // the previous reads of the box are done
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -1488,7 +1507,7 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         if ((EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) && p.amax_ws && lane == 0 && tensor_amax)
             atomicMax(&p.amax_ws[0], tensor_amax);
     }
-    if ((is_store(EPI) || EPI == EPI_SWIGLU_FWD) && warp >= 2 && lane == 0)
+    if ((is_store(EPI) || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) && warp >= 2 && lane == 0)
         bulk_wait_all();  // TMA stores done with shared memory
     if (Cfg<NV, BN, EPI, P2>::BWD_PREFETCH && warp >= 2 && warp < 2 + EW) cp_async_wait_all();
     tc_fence_before();
@@ -1591,6 +1610,11 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
     memset(&tsb, 0, sizeof tsb);
     memset(&tx, 0, sizeof tx);
     memset(&ty, 0, sizeof ty);
+    // the SwiGLU taps' maps: the forward's h in the output map's slot, the
+    // backward's [da1 | da3] and dh in the a1 / a3 slots it does not use
+    if (EPI == EPI_SWIGLU_FWD && g.tap0 && !make_out_map(&tc, g.tap0, g.M, g.f, FP4_OUT_BF16, 64)) return FP4_ERR_CUDA;
+    if (EPI == EPI_SWIGLU_BWD && g.tap1 && !make_out_map(&tx, g.tap1, g.M, 2 * g.f, FP4_OUT_BF16, 64)) return FP4_ERR_CUDA;
+    if (EPI == EPI_SWIGLU_BWD && g.tap0 && !make_out_map(&ty, g.tap0, g.M, g.f, FP4_OUT_BF16, 64)) return FP4_ERR_CUDA;
     if (EPI == EPI_SWIGLU_FWD && (!make_out_map(&tx, g.a1, g.M, g.f, FP4_OUT_BF16, 64) ||
                                   !make_out_map(&ty, g.a3, g.M, g.f, FP4_OUT_BF16, 64)))
         return FP4_ERR_CUDA;
