@@ -645,7 +645,7 @@ struct Cfg {
     // tiles, and the a1 / a3 prefetch slots
     static constexpr int STAGING =
         is_store(EPI)          ? EPI_WARPS * OUT_BUFS * OUT_BOX
-        : EPI == EPI_QKV_ROPE  ? 0
+        : EPI == EPI_QKV_ROPE  ? EPI_WARPS * 1024
         : EPI == EPI_SWIGLU_FWD ? epi_warps(EPI) * FWD_BOX + 4 * 512
                                : epi_warps(EPI) * FWD_BOX + 2 * 4 * 512 + PREFETCH_BYTES;
     static constexpr int STAGES = fit(STAGING);
@@ -1165,7 +1165,8 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
             } else if constexpr (EPI == EPI_QKV_ROPE) {
                 // this thread's 128 columns are exactly one head of token m:
                 // bf16(acc), RoPE on Q and K heads (rotate-half pairs (i, i+64),
-                // binary32 products and sums, then bf16), head-major store
+                // binary32 products and sums, then bf16), head-major TMA stores
+                // (direct 16-byte stores from the lanes were 4-7 % slower)
                 uint32_t pk[64];  // bf16x2 of the head's 128 values
                 {
                     uint32_t r[128];
@@ -1182,14 +1183,8 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                 }
                 const int head = (int)((n0 >> 7) + half);
                 const int hqk = p.heads_q + p.heads_kv;
-                uint16_t* dst;
-                if (head < p.heads_q)
-                    dst = p.q_out + ((int64_t)head * p.M + m) * 128;
-                else if (head < hqk)
-                    dst = p.k_out + ((int64_t)(head - p.heads_q) * p.M + m) * 128;
-                else
-                    dst = p.v_out + ((int64_t)(head - hqk) * p.M + m) * 128;
                 if (head < hqk) {
+                    // RoPE in place: pair (i, i + 64) of the head is words (j, 32 + j)
                     const int64_t pos = m % p.seq_len;
                     const float4* cp = reinterpret_cast<const float4*>(p.rope_cos + pos * 64);
                     const float4* sp = reinterpret_cast<const float4*>(p.rope_sin + pos * 64);
@@ -1198,7 +1193,6 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                         const float4 c0 = cp[2 * g], c1 = cp[2 * g + 1], s0 = sp[2 * g], s1 = sp[2 * g + 1];
                         const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                         const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                        uint32_t lo[4], hi[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const uint32_t wa = pk[4 * g + j], wb = pk[32 + 4 * g + j];
@@ -1211,16 +1205,32 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
                                 l[e] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
                                 h[e] = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
                             }
-                            lo[j] = bf16x2_rn(l[0], l[1]);
-                            hi[j] = bf16x2_rn(h[0], h[1]);
+                            pk[4 * g + j] = bf16x2_rn(l[0], l[1]);
+                            pk[32 + 4 * g + j] = bf16x2_rn(h[0], h[1]);
                         }
-                        *reinterpret_cast<uint4*>(dst + 8 * g) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        *reinterpret_cast<uint4*>(dst + 64 + 8 * g) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     }
-                } else {
+                }
+                // head-major rows: this warp's 32 tokens of one head are 32
+                // consecutive rows of the [heads * M][128] view, stored as eight
+                // 32-row x 32-byte boxes through the warp's 1 KB buffer
+                const CUtensorMap* map = head < p.heads_q ? &tmC : head < hqk ? &tmX : &tmY;
+                const int hl = head < p.heads_q ? head : head < hqk ? head - p.heads_q : head - hqk;
+                const int row0 = (int)((int64_t)hl * p.M + m0 + q * 32);
+                uint8_t* buf = staging + (warp - 2) * 1024;
 #pragma unroll
-                    for (int i = 0; i < 64; i += 4)
-                        *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+                for (int b = 0; b < 8; ++b) {
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        *reinterpret_cast<uint4*>(buf + lane * 32 + ((k ^ ((lane >> 2) & 1)) << 4)) =
+                            make_uint4(pk[8 * b + 4 * k], pk[8 * b + 4 * k + 1], pk[8 * b + 4 * k + 2], pk[8 * b + 4 * k + 3]);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(map, buf, 16 * b, row0);
+                        bulk_commit();
+                    }
                 }
             } else if constexpr (EPI == EPI_SWIGLU_FWD) {
                 // This thread: row lr, output columns [oc, oc + 32) of the
@@ -1507,7 +1517,8 @@ __global__ void __launch_bounds__(kthreads(EPI), 1)
         if ((EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) && p.amax_ws && lane == 0 && tensor_amax)
             atomicMax(&p.amax_ws[0], tensor_amax);
     }
-    if ((is_store(EPI) || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) && warp >= 2 && lane == 0)
+    if ((is_store(EPI) || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD || EPI == EPI_QKV_ROPE) && warp >= 2 &&
+        lane == 0)
         bulk_wait_all();  // TMA stores done with shared memory
     if (Cfg<NV, BN, EPI, P2>::BWD_PREFETCH && warp >= 2 && warp < 2 + EW) cp_async_wait_all();
     tc_fence_before();
@@ -1610,6 +1621,11 @@ int launch_t(const GemmParams& g, const KParams& kp, int64_t n_units, cudaStream
     memset(&tsb, 0, sizeof tsb);
     memset(&tx, 0, sizeof tx);
     memset(&ty, 0, sizeof ty);
+    // QKV + RoPE: q, k, v as [heads * M][128] views with 32-byte row boxes
+    if (EPI == EPI_QKV_ROPE && (!make_out_map(&tc, g.q_out, (int64_t)g.heads_q * g.M, 128, FP4_OUT_BF16, 32) ||
+                                !make_out_map(&tx, g.k_out, (int64_t)g.heads_kv * g.M, 128, FP4_OUT_BF16, 32) ||
+                                !make_out_map(&ty, g.v_out, (int64_t)g.heads_kv * g.M, 128, FP4_OUT_BF16, 32)))
+        return FP4_ERR_CUDA;
     // the SwiGLU taps' maps: the forward's h in the output map's slot, the
     // backward's [da1 | da3] and dh in the a1 / a3 slots it does not use
     if (EPI == EPI_SWIGLU_FWD && g.tap0 && !make_out_map(&tc, g.tap0, g.M, g.f, FP4_OUT_BF16, 64)) return FP4_ERR_CUDA;
