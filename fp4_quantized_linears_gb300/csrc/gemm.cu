@@ -342,41 +342,6 @@ FP4_DEV void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t* a, uint32_t* b) {
         : "r"(ta), "r"(tb)
         : "memory");
 }
-// Two 64-column loads (at ta and tb) under one wait.
-FP4_DEV void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t* a, uint32_t* b) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
-        "}, [%128];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-        "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
-        "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
-        "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
-        "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127"
-        "}, [%129];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
-          "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
-          "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
-          "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
-          "=r"(a[32]), "=r"(a[33]), "=r"(a[34]), "=r"(a[35]), "=r"(a[36]), "=r"(a[37]), "=r"(a[38]), "=r"(a[39]),
-          "=r"(a[40]), "=r"(a[41]), "=r"(a[42]), "=r"(a[43]), "=r"(a[44]), "=r"(a[45]), "=r"(a[46]), "=r"(a[47]),
-          "=r"(a[48]), "=r"(a[49]), "=r"(a[50]), "=r"(a[51]), "=r"(a[52]), "=r"(a[53]), "=r"(a[54]), "=r"(a[55]),
-          "=r"(a[56]), "=r"(a[57]), "=r"(a[58]), "=r"(a[59]), "=r"(a[60]), "=r"(a[61]), "=r"(a[62]), "=r"(a[63]),
-          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
-          "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]),
-          "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]),
-          "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31]),
-          "=r"(b[32]), "=r"(b[33]), "=r"(b[34]), "=r"(b[35]), "=r"(b[36]), "=r"(b[37]), "=r"(b[38]), "=r"(b[39]),
-          "=r"(b[40]), "=r"(b[41]), "=r"(b[42]), "=r"(b[43]), "=r"(b[44]), "=r"(b[45]), "=r"(b[46]), "=r"(b[47]),
-          "=r"(b[48]), "=r"(b[49]), "=r"(b[50]), "=r"(b[51]), "=r"(b[52]), "=r"(b[53]), "=r"(b[54]), "=r"(b[55]),
-          "=r"(b[56]), "=r"(b[57]), "=r"(b[58]), "=r"(b[59]), "=r"(b[60]), "=r"(b[61]), "=r"(b[62]), "=r"(b[63])
-        : "r"(ta), "r"(tb)
-        : "memory");
-}
 FP4_DEV void tmem_ld128(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
@@ -416,30 +381,9 @@ FP4_DEV void tmem_ld128(uint32_t taddr, uint32_t* r) {
 FP4_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
-constexpr int ST_LDS = 136;  // staging row stride (bf16 elements)
 
 FP4_DEV int atom_off(int r, int j) { return (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
 
-// MX row/column block of 32 values: scale byte and 16 bytes of RN codes.
-FP4_DEV uint32_t mx_block_rn(const float* v, uint4& packed) {
-    float amf = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) amf = max3_abs_nan(amf, v[i], v[i + 1]);
-    const uint32_t am = __float_as_uint(amf);
-    if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
-    const int e = e8m0_exponent_up(am);
-    const float mult = exp2_neg(e);
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        float s8[8];
-#pragma unroll
-        for (int b = 0; b < 8; b += 2) f32x2_mul(s8[b], s8[b + 1], v[q * 8 + b], v[q * 8 + b + 1], mult, mult);
-        w[q] = e2m1x8_rn(s8[0], s8[1], s8[2], s8[3], s8[4], s8[5], s8[6], s8[7]);
-    }
-    packed = make_uint4(w[0], w[1], w[2], w[3]);
-    return (uint32_t)(e + 127);
-}
 
 // Largest |bf16| of n words, as fp32 bits, reduced over the warp.
 template <int N>
@@ -498,27 +442,6 @@ FP4_DEV uint32_t mx_words_rn(const uint32_t* w, uint4& packed) {
     return (uint32_t)(e + 127);
 }
 
-// MX block of the low (h = 0) or high (h = 1) bf16 lanes of 32 words, round
-// to nearest; am = fp32 bits of the block's maximum magnitude.
-FP4_DEV uint32_t mx_lane_rn(const uint32_t* w, int h, uint32_t am, uint4& packed) {
-    if (am >= 0x7F800000u) set_status(&g_status_gemm, FP4_ERR_NONFINITE);
-    const int e = e8m0_exponent_up(am);
-    const float mult = exp2_neg(e);
-    uint32_t out[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        float s8[8];
-#pragma unroll
-        for (int b = 0; b < 8; b += 2) {
-            const int i = q * 8 + b;
-            f32x2_mul(s8[b], s8[b + 1], h ? bf16_hi(w[i]) : bf16_lo(w[i]), h ? bf16_hi(w[i + 1]) : bf16_lo(w[i + 1]),
-                      mult, mult);
-        }
-        out[q] = e2m1x8_rn(s8[0], s8[1], s8[2], s8[3], s8[4], s8[5], s8[6], s8[7]);
-    }
-    packed = make_uint4(out[0], out[1], out[2], out[3]);
-    return (uint32_t)(e + 127);
-}
 
 // Two binary32 values rounded to nearest-even bf16 and packed (lo in the low
 // half), one conversion instruction; the same rounding as f32_to_bf16_rn.
